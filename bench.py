@@ -1,0 +1,526 @@
+#!/usr/bin/env python
+"""Benchmark of the fused ZeRO synchronisation-and-update step on one GB300.
+
+Workload (default): the 1.3B-parameter GPT-shaped tensor list (24 layers,
+d = 2048, d_ffn = 8192, vocab 50304; n = 1,311,227,904), P = 8 logical ranks
+in one GPU's memory, bf16 gradients ~ N(0, sigma_T) with sigma_T
+log-uniform in [1e-5, 1e-2] per tensor, fresh fp32 master/m/v.  One step is
+one zdp_step over the whole model (reduce-scatter in ring order, AdamW on
+every shard, bf16 cast, all-gather into all 8 replicas) plus the reset of the
+overflow flag and gradient sum of squares it reports.
+
+Prints one JSON line.  `value` is whole-job parameters per second with the
+inputs resident in HBM (CUDA events on the step's stream, max over ranks);
+`e2e` is the same metric through the same C ABI with the gradients copied
+from pinned host memory every step and the step's flag and sum of squares
+read back; `roofline` relates the fused kernel's algorithmic bytes,
+(4P + 24) per parameter, to the measured HBM copy bandwidth; `cpu_baseline`
+times the CPU oracle on a bounded slice of the same workload.
+
+--impl reference times the CPU oracle alone on the same workload (a bounded
+slice per step), as the reference arm.
+
+Under torchrun with N > 1 every rank runs its own replica of the workload on
+its own GPU (the step needs no exchange between GPUs: its P ranks live in
+one HBM), and `value` counts all ranks' parameters over the slowest rank's
+time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO step params/s and achieved HBM TB/s vs roofline (1.3B params, P=8, 1 GB300)"
+HP = dict(lr=1e-4, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("zero_gradient_reduce_gb300/csrc/zdp_kernels.cuh",
+                  "zero_gradient_reduce_gb300/csrc/kernels_grad.inc")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="gpt_1p3b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--e2e-bucket", type=int, default=1 << 26,
+                    help="elements per rank per host->device copy bucket in the e2e leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-sample", type=int, default=1 << 24,
+                    help="parameters per oracle step in the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def bytes_per_param(P: int) -> int:
+    # P bf16 gradient reads + fp32 master/m/v read and written + P bf16 replica writes
+    return 2 * P + 12 + 12 + 2 * P
+
+
+def config_of(wl, bucket_elems=0):
+    return {
+        "workload": wl.name,
+        "n_params": wl.n,
+        "P": wl.P,
+        "shard": -(-wl.n // wl.P),
+        "tensors": len(wl.tensors),
+        "grad_dtype": wl.grad_dtype,
+        "state": "fp32 master/m/v, bf16 replicas",
+        "bucket_elems": bucket_elems,
+        "check_overflow": False,
+        "outputs": "overflow flag + fp64 grad sum of squares",
+        "l2": "no flush: every step streams (4P+24)n bytes, far above the 129 MB L2",
+        "parallelism": "P logical ZeRO ranks in one GPU; replicas per GPU when n_gpus > 1",
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"zdp_fused_step_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m1 = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m2 = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not m1 or not m2 or m2.group(1) != kernel_source_hash():
+        return None
+    return float(m1.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        reasons = set()
+        for p in inside:
+            for name, val in zip(self.NAMES, p[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+def gpu_id_for_smi(local_rank: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[local_rank]
+        return str(local_rank)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from zero_gradient_reduce_gb300 import workloads, zdp
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    zdp.load()
+
+    wl = workloads.by_name(args.workload)
+    P, n = wl.P, wl.n
+    S = -(-n // P)
+    n_pad = P * S
+    seed = args.seed + 1000 * rank
+
+    grads = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    for q in range(P):
+        workloads.fill_grads(grads[q], wl, q, 0, seed)
+    state = torch.empty(3, n_pad, dtype=torch.float32, device=dev)
+    master, m, v = state[0], state[1], state[2]
+    workloads.fill_state(master, m, v, wl, seed)
+    replicas = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    words = torch.zeros(16, dtype=torch.uint8, device=dev)
+    flag = words[0:4].view(torch.int32)
+    sumsq = words[8:16].view(torch.float64)
+    torch.cuda.synchronize()
+
+    a, keep = zdp.make_step_args(grads, master, m, v, replicas, n=n, scale=wl.scale, t=1,
+                                 d_overflow=flag, d_sumsq=sumsq, **HP)
+    launches_per_step = 1  # one fused launch over the whole range (no buckets, no check)
+    stream = torch.cuda.current_stream(dev)
+    t = 0
+
+    def one_step(e0=None, e1=None):
+        nonlocal t
+        t += 1
+        a.t = t
+        words.zero_()
+        if e0 is not None:
+            e0.record(stream)
+        zdp.zdp_step(a, stream)
+        if e1 is not None:
+            e1.record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_id_for_smi(local_rank))
+    sampler.start()
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        one_step(ev0[k], ev1[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    kernel_ms = sum(ev0[k].elapsed_time(ev1[k]) for k in range(K)) / K
+    step_flag = int(flag.item())
+    times = torch.tensor([elapsed_ms, kernel_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms, kernel_ms = float(times[0]), float(times[1])
+    ms_per_step = elapsed_ms / K
+    value = world * n * K / (elapsed_ms / 1e3)
+
+    # ---- end to end through the C ABI: gradients from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t)
+        if world > 1:
+            x = torch.tensor([e2e.get("seconds_per_step") or 0.0], dtype=torch.float64,
+                             device=dev)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            if e2e.get("value") is not None:
+                e2e["value"] = world * n / float(x[0])
+        e2e.pop("seconds_per_step", None)
+
+    out = None
+    if rank == 0:
+        peak, peak_kind = measured_peak()
+        alg_bytes = bytes_per_param(P) * n
+        achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+        traffic = recorded_traffic(wl.name)
+        clocks = sampler.summary(wall0, wall1)
+        out = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "params/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic: seeded N(0, sigma_T) bf16 gradients (sigma_T log-uniform "
+                    "[1e-5, 1e-2] per tensor), master ~ N(0, 0.02), m = v = 0 at t = 1",
+            "config": config_of(wl),
+            "hbm_tbs": alg_bytes / (ms_per_step / 1e3) / 1e12,
+            "roofline": {
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": traffic,
+                "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "kernel": f"k_fused<P={P}, bf16>",
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "kernel_ms": kernel_ms,
+            },
+            "gpu_launches": K * launches_per_step,
+            "clocks": clocks,
+            "overflow_flag": step_flag,
+        }
+        if e2e is not None:
+            out["e2e"] = e2e
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(args, wl, grads, state, P, n)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t0):
+    """Gradients copied host->device every step (bucket by bucket on a copy
+    stream, overlapped with zdp_step on the previous bucket), flag and sum of
+    squares read back to the host; wall clock over whole steps."""
+    import torch
+
+    from zero_gradient_reduce_gb300 import zdp
+
+    P, n = wl.P, wl.n
+    try:
+        host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
+    except RuntimeError as e:
+        return {"value": None, "unit": "params/s", "unavailable": f"pinned host memory: {e}"[:200]}
+    for q in range(P):
+        host[q].copy_(grads[q])
+    host_words = torch.empty(16, dtype=torch.uint8, pin_memory=True)
+    B = max(1, args.e2e_bucket)
+    bounds = [(lo, min(n, lo + B)) for lo in range(0, n, B)]
+    argv = []
+    for lo, hi in bounds:
+        a, keep = zdp.make_step_args([g[lo:hi] for g in grads], master, m, v, replicas, n=n,
+                                     scale=wl.scale, t=1, off=lo, length=hi - lo,
+                                     d_overflow=flag, d_sumsq=sumsq, **HP)
+        argv.append((a, keep))
+    main = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    t = t0
+
+    def step():
+        nonlocal t
+        t += 1
+        words.zero_()
+        done = [torch.cuda.Event() for _ in bounds]
+        copy.wait_stream(main)
+        for (lo, hi), ev in zip(bounds, done):
+            with torch.cuda.stream(copy):
+                for q in range(P):
+                    grads[q][lo:hi].copy_(host[q][lo:hi], non_blocking=True)
+            ev.record(copy)
+        for (a, _), ev in zip(argv, done):
+            main.wait_event(ev)
+            a.t = t
+            zdp.zdp_step(a, main)
+        host_words.copy_(words, non_blocking=True)
+        main.synchronize()
+        return int(host_words[0:4].view(torch.int32)[0])
+
+    step()  # warm-up
+    K = max(1, args.e2e_steps)
+    t_start = time.perf_counter()
+    for _ in range(K):
+        step()
+    secs = (time.perf_counter() - t_start) / K
+    return {"value": n / secs, "unit": "params/s", "h2d_bytes_per_step": 2 * P * n,
+            "d2h_bytes_per_step": 16, "steps": K, "bucket_elems": B,
+            "gpu_launches_per_step": len(bounds), "seconds_per_step": secs}
+
+
+def _oracle_slice(P, S, n, length):
+    lo = max(0, min(S - length // 2, n - length))
+    return lo, min(length, n - lo)
+
+
+def cpu_baseline(args, wl, grads, state, P, n):
+    """The CPU oracle, as it is, on one host core, over a slice of the same
+    workload straddling the boundary between rank 0's and rank 1's shards."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    S = -(-n // P)
+    lo, length = _oracle_slice(P, S, n, args.cpu_sample)
+    g = np.stack([grads[q][lo:lo + length].view(torch.int16).cpu().numpy().view(np.uint16)
+                  for q in range(P)])
+    w, m, v = (state[k, lo:lo + length].cpu().numpy().copy() for k in range(3))
+    rep = np.empty((P, length), np.uint16)
+    oracle.build()
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.step(g, oracle.BF16, w, m, v, rep, n, lo, length, wl.scale, t=steps + 1,
+                    base=lo, **HP)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= args.cpu_seconds:
+            break
+    return {"value": steps * length / el, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "host_cores": os.cpu_count(),
+            "sample": f"{steps} oracle steps over params [{lo}, {lo + length}) of {wl.name} "
+                      f"(P={P}, straddling the rank 0/1 shard boundary), {el:.1f} s"}
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The CPU oracle timed on the host, on the same workload and metric: each
+    step is one oracle step over a bounded slice of the model."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from zero_gradient_reduce_gb300 import workloads
+
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    wl = workloads.by_name(args.workload)
+    P, n = wl.P, wl.n
+    S = -(-n // P)
+    lo, length = _oracle_slice(P, S, n, args.cpu_sample)
+    g = np.stack([workloads.fill_grads(torch.empty(length, dtype=torch.bfloat16), wl, q, 0,
+                                       args.seed, lo).view(torch.int16).numpy().view(np.uint16)
+                  for q in range(P)])
+    gen = torch.Generator().manual_seed(workloads.key(args.seed, workloads.STREAM_MASTER))
+    w = (torch.randn(length, generator=gen) * 0.02).numpy().astype(np.float32)
+    m = np.zeros(length, np.float32)
+    v = np.zeros(length, np.float32)
+    rep = np.empty((P, length), np.uint16)
+    oracle.build()
+    t = 0
+
+    def step():
+        nonlocal t
+        t += 1
+        oracle.step(g, oracle.BF16, w, m, v, rep, n, lo, length, wl.scale, t=t, base=lo, **HP)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = args.steps * length / el
+    sample = (f"each step: one oracle step over params [{lo}, {lo + length}) of {wl.name} "
+              f"(P={P}), single-threaded")
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3 * (n / length),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic: seeded bf16 gradients and fp32 state of the same distributions",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "host_cores": os.cpu_count(), "sample": sample},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * zdp.h -- C ABI of libzdp, the ZeRO synchronisation-and-update step on one
+ * GPU.  P logical data-parallel ranks keep their gradients and parameter
+ * replicas as separate buffers in one GPU's memory.  One step
+ *   1. reduce-scatters the P gradients: element i is owned by rank
+ *      r = i / S, S = ceil(n / P), and summed in fp32 in ring order,
+ *      starting with rank (r+1) mod P and ending with rank r, then multiplied
+ *      by `scale`;
+ *   2. applies AdamW to the owner's shard of the fp32 master weight, first
+ *      moment m and second moment v;
+ *   3. rounds the new master weight to bf16 (nearest, ties to even) and
+ *   4. all-gathers it into every rank's replica.
+ *
+ * Sources, by page title and section:
+ *  - Fudan MLSys ch. 9 "Distributed training and data parallelism":
+ *    9.2.2 Adam (moment updates, bias correction, epsilon outside the
+ *    square root); 9.3.6 ring all-reduce = ring reduce-scatter (P-1 steps,
+ *    each adding the received partial sum to the local chunk) + ring
+ *    all-gather (P-1 steps, overwrite); 9.4.2 ZeRO-1/2 step
+ *    (reduce-scatter gradients, update the own shard, all-gather params).
+ *  - CS336 Lecture 7 notes "Parallelism I": 3.4 all-reduce = reduce-scatter
+ *    + all-gather; 4.2 ring schedule; 6.2 gradient averaging as SUM then
+ *    divide by world size; 7 the 16 bytes/parameter mixed-precision state
+ *    (bf16 param, bf16 grad, fp32 master, m, v); 8.1 FlatZeRO1 (flatten all
+ *    parameters, split into P equal segments); 11 exercise 1(e) (zero
+ *    padding to a multiple of P).
+ *  - "Must-know: communication cost of LLM training" interview guide, 1.4
+ *    item 6: after a reduce-scatter GPU r holds reduced chunk r.
+ * The pages name AdamW without writing its decay term; this library uses
+ * decoupled decay on the pre-update weight:
+ *   w <- w - (lr*wd)*w - lr * (m_hat / (sqrt(v_hat) + eps)).
+ *
+ * Conventions for every call:
+ *  - The caller owns all memory.  No call allocates or frees device or host
+ *    memory.  Device pointers are plain CUDA device addresses (e.g. a torch
+ *    tensor's data_ptr()).  "Host array of P device pointers" means a
+ *    host-memory array whose entries are device addresses.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream) and never synchronise.
+ *  - Return value: ZDP_OK, or ZDP_ERR_INVALID when an argument check fails
+ *    (detected on the host before anything is enqueued), or ZDP_ERR_CUDA when
+ *    a CUDA call fails.  zdp_last_error() then returns a message (per host
+ *    thread, valid until the thread's next call).
+ *  - Element counts are int64.  P is 1..ZDP_MAX_P.
+ *  - A non-finite reduced gradient is data, not an error: it is reported
+ *    through the optional device overflow word.
+ *  - Any 2-byte (bf16/fp16) or 4-byte (fp32) aligned pointer is accepted.
+ *    When every buffer's element 0 sits on a 16-byte boundary (torch's
+ *    allocations do) the kernels move 16 bytes per access; otherwise a
+ *    slower one-element-per-access kernel runs, with identical results.
+ *  - Output buffers must not overlap inputs or each other; overlapping
+ *    ranges are rejected with ZDP_ERR_INVALID.
+ */
+#ifndef ZDP_H
+#define ZDP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zdp_dtype {
+  ZDP_BF16 = 0, /* bfloat16 gradients */
+  ZDP_FP16 = 1  /* IEEE binary16 gradients (loss-scaled training) */
+} zdp_dtype;
+
+enum {
+  ZDP_OK = 0,
+  ZDP_ERR_INVALID = -1,
+  ZDP_ERR_CUDA = -2,
+  ZDP_MAX_P = 64
+};
+
+/* Library version, e.g. 100 for 0.1.0. */
+int zdp_version(void);
+
+/* Shard size S = ceil(n / P): rank r owns flat elements [r*S, (r+1)*S);
+ * elements at or beyond n are zero padding (CS336 Lecture 7 notes,
+ * exercise 1(e); FlatZeRO1 in 8.1).  Returns -1 if n < 1 or P is outside
+ * 1..ZDP_MAX_P.  Pure host function. */
+int64_t zdp_shard_size(int64_t n, int P);
+
+/* Reduce-scatter (step 1 alone).
+ *   grads      host array of P device pointers; grads[q] holds rank q's n
+ *              gradients (bf16 or fp16 per gdt).
+ *   shards     device fp32 output of P*S elements: shards[i] is the ring-order
+ *              sum of element i times `scale` for i < n, and 0.0 for the
+ *              padding i in [n, P*S).  Rank r's shard is shards + r*S.
+ *   d_overflow nullable device int32; OR-ed with 1 if any shards[i] is not
+ *              finite (never cleared by the call).
+ *   d_sumsq    nullable device double; the fp64 sum of shards[i]^2 is added
+ *              to it (never cleared by the call).
+ * Source: Fudan MLSys ch. 9, 9.3.6 (reduce-scatter phase of the ring);
+ * the interview guide 1.4 item 6 (rank r keeps chunk r). */
+int zdp_reduce_scatter(const void* const* grads, int gdt, float* shards, int64_t n, int P,
+                       float scale, int32_t* d_overflow, double* d_sumsq, void* stream);
+
+/* AdamW on one shard (step 2 alone), elementwise over `count` elements:
+ *   m <- b1*m + (1-b1)*g;  v <- b2*v + (1-b2)*g*g;
+ *   u  = (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps);
+ *   w <- w - (lr*wd)*w;  w <- w - lr*u.
+ * Every operation is one IEEE fp32 operation rounded to nearest (no fused
+ * multiply-add); 1-b^t is evaluated in double and rounded to fp32.
+ *   master, m, v  device fp32, count elements each, updated in place.
+ *   grad_shard    device fp32, count elements (e.g. a zdp_reduce_scatter shard).
+ *   t             step number, >= 1.
+ * Source: Fudan MLSys ch. 9, 9.2.2. */
+int zdp_adamw_shard(float* master, float* m, float* v, const float* grad_shard, int64_t count,
+                    float lr, float b1, float b2, float eps, float wd, int t, void* stream);
+
+/* All-gather of the updated parameters (steps 3 and 4 alone): for i < n and
+ * every rank q, replicas[q][i] = bf16(master[i]), rounded to nearest even.
+ *   master    device fp32, at least n elements (the concatenated shards).
+ *   replicas  host array of P device pointers, n bf16 (uint16) each.
+ * Source: Fudan MLSys ch. 9, 9.3.6 (all-gather phase: overwrite only);
+ * CS336 Lecture 7 notes 8.1 step 4 (all-gather the parameters). */
+int zdp_all_gather(const float* master, uint16_t* const* replicas, int64_t n, int P,
+                   void* stream);
+
+/* Arguments of the fused step. */
+typedef struct zdp_step_args {
+  const void* const* grads;   /* host array of P device pointers; grads[q][j] is rank
+                                 q's gradient of global element off+j, j < len */
+  int gdt;                    /* zdp_dtype of the gradients */
+  float* master;              /* device fp32, >= n elements, indexed by global element */
+  float* m;                   /* device fp32, >= n elements */
+  float* v;                   /* device fp32, >= n elements */
+  uint16_t* const* replicas;  /* host array of P device pointers, >= n bf16 each,
+                                 indexed by global element */
+  int64_t n;                  /* model size; fixes S = ceil(n/P) and so the owners */
+  int64_t off;                /* first global element this call processes */
+  int64_t len;                /* number of elements this call processes (may be 0) */
+  int P;                      /* logical ranks, 1..ZDP_MAX_P */
+  float scale;                /* multiplies the ring sum, e.g. 1/P or 1/(P*loss_scale) */
+  float lr, b1, b2, eps, wd;  /* AdamW hyper-parameters */
+  int t;                      /* AdamW step number, >= 1 */
+  int64_t bucket_elems;       /* > 0: walk [off, off+len) in buckets of this many
+                                 elements (one launch each); 0: whole range at once */
+  int check_overflow;         /* nonzero: if any reduced gradient in the range is not
+                                 finite, write nothing to master/m/v/replicas */
+  int32_t* d_overflow;        /* nullable device int32, OR-ed with 1 on a non-finite
+                                 reduced gradient in the range */
+  double* d_sumsq;            /* nullable device double; the fp64 sum of squares of
+                                 the reduced gradients of the range is added */
+  void* workspace;            /* device scratch for check_overflow (else unused), at
+                                 least zdp_step_workspace_bytes() bytes, 16-B aligned */
+  size_t workspace_bytes;
+} zdp_step_args;
+
+/* Scratch bytes zdp_step needs for these arguments: 0 without
+ * check_overflow, else 4*len rounded up to 256, plus 256. */
+size_t zdp_step_workspace_bytes(const zdp_step_args* args);
+
+/* The fused step over global elements [off, off+len): reduce-scatter, AdamW,
+ * bf16 cast and all-gather in one pass over memory (CS336 Lecture 7 notes
+ * 8.1, FlatZeRO1; Fudan MLSys ch. 9, 9.4.2, ZeRO-1/2 step).  Ownership and
+ * summation order depend only on the global index and n, never on off, len
+ * or bucket_elems, so any split of [0, n) into calls or buckets gives
+ * bit-identical results.
+ * With check_overflow the call makes two passes: the first stores the
+ * reduced gradients in the workspace and raises a device flag on any
+ * non-finite value; the second, skipped on the device when the flag is set,
+ * applies AdamW and the all-gather.  The skip decision covers this call's
+ * range only; a caller streaming one step through several calls and wanting
+ * a step-wide skip must check every range first (e.g. with
+ * zdp_reduce_scatter into a scratch buffer).  A skipped step leaves t to the
+ * caller: do not advance it. */
+int zdp_step(const zdp_step_args* args, void* stream);
+
+/* Message for the last non-OK return on this host thread ("" if none). */
+const char* zdp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZDP_H */

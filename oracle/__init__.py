@@ -66,8 +66,8 @@ def _load():
             "ora_adamw": (None, [vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, ctypes.c_int]),
             "ora_all_gather": (None, [vp, vp, i64, i64, ctypes.c_int]),
             "ora_step": (ctypes.c_int, [vp, i64, ctypes.c_int, vp, vp, vp, vp, i64, i64, i64, i64,
-                                        ctypes.c_int, f32, f32, f32, f32, f32, f32, ctypes.c_int,
-                                        ctypes.c_int, vp, vp]),
+                                        i64, ctypes.c_int, f32, f32, f32, f32, f32, f32,
+                                        ctypes.c_int, ctypes.c_int, vp, vp]),
             "ora_step_sampled": (ctypes.c_int, [vp, vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, i64,
                                                 ctypes.c_int, f32, f32, f32, f32, f32, f32,
                                                 ctypes.c_int, ctypes.c_int, vp]),
@@ -181,25 +181,27 @@ def all_gather(master, n: int, P: int) -> np.ndarray:
 
 
 def step(grads, gdt, master, m, v, replicas, n, off, len_, scale, lr, b1, b2, eps, wd, t,
-         check_overflow=False):
+         check_overflow=False, base=0):
     """The fused step on host arrays, in place on master/m/v/replicas.
 
     grads: [P, >=len_] uint16 rows holding elements [off, off+len_).
-    master/m/v: float32 arrays of at least n elements.
-    replicas: [P, >=n] uint16.
+    master/m/v: float32 arrays holding global elements [base, off+len_).
+    replicas: [P, >= off+len_-base] uint16, element i in column i - base.
     Returns (overflow, sumsq).
     """
     g = _gbits(grads)
     P = g.shape[0]
+    assert 0 <= base <= off
+    need = off + len_ - base
     for a in (master, m, v):
-        assert a.dtype == np.float32 and a.flags.c_contiguous and a.size >= n
+        assert a.dtype == np.float32 and a.flags.c_contiguous and a.size >= need
     assert replicas.dtype == np.uint16 and replicas.flags.c_contiguous
-    assert replicas.shape[0] == P and replicas.shape[1] >= n
+    assert replicas.shape[0] == P and replicas.shape[1] >= need
     flag = np.zeros(1, np.int32)
     ss = np.zeros(1, np.float64)
     rc = _load().ora_step(_ptr(g), g.shape[1], gdt, _ptr(master), _ptr(m), _ptr(v),
-                          _ptr(replicas), replicas.shape[1], n, off, len_, P, scale, lr, b1, b2,
-                          eps, wd, t, int(bool(check_overflow)), _ptr(flag), _ptr(ss))
+                          _ptr(replicas), replicas.shape[1], base, n, off, len_, P, scale, lr,
+                          b1, b2, eps, wd, t, int(bool(check_overflow)), _ptr(flag), _ptr(ss))
     if rc != 0:
         raise ValueError("oracle step: bad arguments")
     return int(flag[0]), float(ss[0])

@@ -283,15 +283,16 @@ void ora_all_gather(const float* master, uint16_t* replicas, int64_t rld, int64_
 // ---- the fused step by definition -------------------------------------------
 // Processes the global element range [off, off+len) of an n-element model.
 // grads row q (stride ld) holds rank q's gradient for that range: element
-// off+j is grads[q*ld + j].  master/m/v are indexed by the global element
-// index; replica row q (stride rld) likewise.  With check_overflow != 0 and a
-// non-finite reduced gradient anywhere in the range, nothing is written.
-// Returns 0, or -1 on bad arguments.
+// off+j is grads[q*ld + j].  master/m/v hold global elements from `base` on:
+// element i is master[i - base]; replica row q (stride rld) likewise.  With
+// check_overflow != 0 and a non-finite reduced gradient anywhere in the
+// range, nothing is written.  Returns 0, or -1 on bad arguments.
 int ora_step(const uint16_t* grads, int64_t ld, int gdt, float* master, float* m, float* v,
-             uint16_t* replicas, int64_t rld, int64_t n, int64_t off, int64_t len, int P,
+             uint16_t* replicas, int64_t rld, int64_t base, int64_t n, int64_t off, int64_t len,
+             int P,
              float scale, float lr, float b1, float b2, float eps, float wd, int t,
              int check_overflow, int32_t* overflow, double* sumsq) {
-  if (P < 1 || n < 1 || off < 0 || len < 0 || off + len > n || t < 1) return -1;
+  if (P < 1 || n < 1 || off < 0 || len < 0 || off + len > n || t < 1 || base > off) return -1;
   const int64_t S = shard_size(n, P);
   const Adam a = make_adam(lr, b1, b2, eps, wd, t);
   std::vector<float> vals(P);
@@ -309,10 +310,10 @@ int ora_step(const uint16_t* grads, int64_t ld, int gdt, float* master, float* m
   if (sumsq) *sumsq += ss;
   if (check_overflow && flag) return 0;
   for (int64_t j = 0; j < len; ++j) {
-    const int64_t i = off + j;
-    adamw_element(master[i], m[i], v[i], g[j], a);
-    const uint16_t p = float_to_bf16_rne(master[i]);
-    for (int q = 0; q < P; ++q) replicas[q * rld + i] = p;
+    const int64_t k = off + j - base;
+    adamw_element(master[k], m[k], v[k], g[j], a);
+    const uint16_t p = float_to_bf16_rne(master[k]);
+    for (int q = 0; q < P; ++q) replicas[q * rld + k] = p;
   }
   return 0;
 }

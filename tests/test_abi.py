@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/zdp.h declares, and rejects bad arguments on the host
+before touching CUDA (no call here reaches a kernel launch)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from zero_gradient_reduce_gb300 import build, zdp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "zdp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(zdp_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return zdp.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert set(declared) == set(zdp.EXPORTS)
+    raw = ctypes.CDLL(build.LIB)
+    for name in declared:
+        assert hasattr(raw, name), name
+
+
+def test_pure_host_functions(lib):
+    assert zdp.zdp_version() == 100
+    assert zdp.zdp_shard_size(10, 4) == 3
+    assert zdp.zdp_shard_size(8, 8) == 1
+    assert zdp.zdp_shard_size(1, 64) == 1
+    assert zdp.zdp_shard_size(1_311_227_904, 8) == 163_903_488
+    assert zdp.zdp_shard_size(0, 4) == -1
+    assert zdp.zdp_shard_size(10, 0) == -1
+    assert zdp.zdp_shard_size(10, 65) == -1
+
+
+FAKE = 1 << 40  # an address that is never dereferenced: every call below fails its checks first
+
+
+def _args(**kw):
+    P = kw.pop("P", 2)
+    base = dict(n=1000, scale=0.5, t=1, lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
+    base.update(kw)
+    grads = [FAKE + q * (1 << 20) for q in range(P)]
+    reps = [FAKE + (16 + q) * (1 << 20) for q in range(P)]
+    return zdp.make_step_args(grads, FAKE + (100 << 20), FAKE + (104 << 20),
+                              FAKE + (108 << 20), reps, **base)
+
+
+@pytest.mark.parametrize("mutate,needle", [
+    (lambda a: setattr(a, "P", 0), "P=0"),
+    (lambda a: setattr(a, "P", 65), "P=65"),
+    (lambda a: setattr(a, "n", 0), "n=0"),
+    (lambda a: setattr(a, "t", 0), "t=0"),
+    (lambda a: setattr(a, "off", 999), "outside"),
+    (lambda a: setattr(a, "len", -1), "outside"),
+    (lambda a: setattr(a, "gdt", 7), "gradient type"),
+    (lambda a: setattr(a, "master", None), "NULL"),
+    (lambda a: setattr(a, "master", FAKE + (16 << 20)), "overlap"),
+    (lambda a: setattr(a, "m", FAKE + (100 << 20) + 400), "overlap"),
+    (lambda a: setattr(a, "master", FAKE + (100 << 20) + 2), "aligned"),
+    (lambda a: setattr(a, "check_overflow", 1), "workspace"),
+    (lambda a: setattr(a, "bucket_elems", -5), "bucket"),
+])
+def test_step_rejects_bad_arguments(lib, mutate, needle):
+    a, keep = _args()
+    mutate(a)
+    with pytest.raises(zdp.ZdpError) as e:
+        zdp.zdp_step(a, stream=0)
+    assert e.value.status == zdp.ZDP_ERR_INVALID
+    assert needle in str(e.value)
+
+
+def test_step_rejects_small_workspace(lib):
+    a, keep = _args(check_overflow=True)
+    need = zdp.zdp_step_workspace_bytes(a)
+    assert need == 256 + ((1000 + 8) * 4 + 255) // 256 * 256
+    a.workspace = FAKE + (200 << 20)
+    a.workspace_bytes = need - 1
+    with pytest.raises(zdp.ZdpError, match="workspace of"):
+        zdp.zdp_step(a, stream=0)
+
+
+def test_gradient_overlapping_a_replica_is_rejected(lib):
+    a, keep = _args()
+    g = (ctypes.c_void_p * 2)(FAKE, FAKE + (16 << 20) + 64)  # grads[1] inside replicas[0]
+    a.grads = ctypes.cast(g, ctypes.c_void_p)
+    with pytest.raises(zdp.ZdpError, match="overlap"):
+        zdp.zdp_step(a, stream=0)
+
+
+def test_unfused_calls_reject_bad_arguments(lib):
+    with pytest.raises(zdp.ZdpError, match="P=0"):
+        zdp.zdp_reduce_scatter([], FAKE, 10, 0, 1.0, stream=0)
+    with pytest.raises(zdp.ZdpError, match="overlap"):
+        zdp.zdp_reduce_scatter([FAKE, FAKE + 4096], FAKE + 8, 100, 2, 1.0, stream=0)
+    with pytest.raises(zdp.ZdpError, match="t=0"):
+        zdp.zdp_adamw_shard(FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, 10, 1e-3, 0.9, 0.95,
+                            1e-8, 0.0, 0, stream=0)
+    with pytest.raises(zdp.ZdpError, match="overlap"):
+        zdp.zdp_adamw_shard(FAKE, FAKE + 16, FAKE + 8192, FAKE + 12288, 10, 1e-3, 0.9, 0.95,
+                            1e-8, 0.0, 1, stream=0)
+    with pytest.raises(zdp.ZdpError, match="overlap"):
+        zdp.zdp_all_gather(FAKE, [FAKE + 4096, FAKE + 4096 + 100], 100, 2, stream=0)
+    # count 0 is a valid no-op that never reaches CUDA
+    zdp.zdp_adamw_shard(FAKE, FAKE, FAKE, FAKE, 0, 1e-3, 0.9, 0.95, 1e-8, 0.0, 1, stream=0)
+
+
+def test_zero_length_step_is_a_host_no_op(lib):
+    a, keep = _args(off=10, length=0)
+    zdp.zdp_step(a, stream=0)

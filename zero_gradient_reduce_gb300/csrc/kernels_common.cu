@@ -1,0 +1,72 @@
+// Kernels that do not read rank gradients (AdamW from reduced gradients,
+// cast + all-gather), the per-type dispatch, and grid sizing.
+#include <mutex>
+#include <unordered_map>
+
+#include "zdp_kernels.cuh"
+
+namespace zdp {
+
+cudaError_t launch_fused_bf16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_fused_fp16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_reduce_bf16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_reduce_fp16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
+
+int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms) {
+  const int64_t work = vec ? (p.hi + kVec - 1) / kVec - p.lo / kVec : p.hi - p.lo;
+  if (work <= 0) return 0;
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> resident;
+  int occ = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = resident.find(kernel);
+    if (it != resident.end()) {
+      occ = it->second;
+    } else {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess
+          || occ < 1) {
+        occ = 1;
+      }
+      resident[kernel] = occ;
+    }
+  }
+  const int64_t full = static_cast<int64_t>(num_sms) * occ;
+  const int64_t need = (work + kThreads - 1) / kThreads;
+  return static_cast<int>(need < full ? need : full);
+}
+
+namespace {
+cudaError_t launch_fn(const void* fn, const KParams& p, bool vec, int num_sms, cudaStream_t s) {
+  const int grid = grid_for(fn, p, vec, num_sms);
+  if (grid == 0) return cudaSuccess;
+  void* args[] = {const_cast<KParams*>(&p)};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, s);
+}
+}  // namespace
+
+cudaError_t launch_fused(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
+                         cudaStream_t s) {
+  return gdt == ZDP_BF16 ? launch_fused_bf16(p, sumsq, vec, num_sms, s)
+                         : launch_fused_fp16(p, sumsq, vec, num_sms, s);
+}
+
+cudaError_t launch_reduce(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
+                          cudaStream_t s) {
+  return gdt == ZDP_BF16 ? launch_reduce_bf16(p, sumsq, vec, num_sms, s)
+                         : launch_reduce_fp16(p, sumsq, vec, num_sms, s);
+}
+
+cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
+  const void* fn = vec ? reinterpret_cast<const void*>(&k_adam_gather<true>)
+                       : reinterpret_cast<const void*>(&k_adam_gather<false>);
+  return launch_fn(fn, p, vec, num_sms, s);
+}
+
+cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
+  const void* fn = vec ? reinterpret_cast<const void*>(&k_gather<true>)
+                       : reinterpret_cast<const void*>(&k_gather<false>);
+  return launch_fn(fn, p, vec, num_sms, s);
+}
+
+}  // namespace zdp

@@ -1,0 +1,64 @@
+// zdp_internal.h -- declarations shared by the host API (zdp_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zdp.h"
+
+namespace zdp {
+
+constexpr int kThreads = 256;  // threads per block of every kernel
+constexpr int kVec = 8;        // elements per vector: 16 B of bf16, 32 B of fp32
+
+// AdamW constants, prepared once per call on the host.
+struct AdamK {
+  float lr, b1, b2, eps;
+  float one_minus_b1, one_minus_b2;  // fp32 1-b1, 1-b2
+  float lr_wd;                       // fp32 lr*wd
+  float bc1, bc2;                    // fp32 rounding of the double 1-b^t
+};
+
+// Everything a kernel needs, passed by value as a __grid_constant__ parameter.
+// Element indices are global (0..n); each pointer family says how it maps a
+// global index to an address.
+struct KParams {
+  // rank q's gradient of global element i: g[q] + (i - goff) * esize
+  const void* g[ZDP_MAX_P];
+  // rank q's replica of global element i: rep[q][i]
+  uint16_t* rep[ZDP_MAX_P];
+  float* w;  // master: w[i]
+  float* m;  // first moment: m[i]
+  float* v;  // second moment: v[i]
+  const float* gin;  // reduced gradient input: gin[i - gin_base]
+  float* gout;       // reduced gradient output: gout[i - gout_base]
+  int64_t goff, gin_base, gout_base;
+  int64_t S;       // shard size; owner of i is i / S
+  int64_t lo, hi;  // this launch processes global elements [lo, hi)
+  float inv_s;     // fp32 1/S, for the owner estimate
+  int P;           // ranks whose gradients are summed
+  int nrep;        // replicas written (0..P)
+  float scale;
+  AdamK ad;
+  int32_t* flag;       // nullable: OR-ed with 1 on a non-finite reduced gradient
+  double* sumsq;       // nullable: fp64 sum of squares of reduced gradients added
+  const int32_t* gate; // nullable: when *gate != 0 the launch writes nothing
+};
+
+// Launchers, one per kernel family.  `vec` selects the 16-byte-access
+// kernels (every buffer's element 0 on a 16-byte boundary).  The grid is a
+// persistent grid-stride grid: `num_sms` times the kernel's resident blocks
+// per SM, capped by the work.  Each returns the launch status.
+cudaError_t launch_fused(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
+                         cudaStream_t s);
+cudaError_t launch_reduce(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
+                          cudaStream_t s);
+cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+
+// Grid size for `kernel` over the elements [p.lo, p.hi): resident blocks per
+// SM (queried once per kernel and cached) times num_sms, capped by the work.
+int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms);
+
+}  // namespace zdp
