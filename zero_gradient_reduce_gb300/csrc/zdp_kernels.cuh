@@ -84,7 +84,8 @@ __device__ __forceinline__ int owner_of(int64_t i, const KParams& p, int P) {
   } else if (static_cast<int64_t>(r + 1) * p.S <= i) {
     ++r;
   }
-  return r;
+  // i < n <= P*S keeps r in [0, P-1]; the clamp makes that hold for any input.
+  return r < 0 ? 0 : (r > P - 1 ? P - 1 : r);
 }
 
 // ---------------------------------------------------------------------------
