@@ -60,9 +60,10 @@ def assert_state_close(got: np.ndarray, want: np.ndarray, what: str) -> float:
     assert np.array_equal(nan_g, nan_w), f"{what}: NaN positions differ"
     ok = ~nan_w
     g64, w64 = got[ok].astype(np.float64), want[ok].astype(np.float64)
-    same_inf = np.isinf(w64) & (g64 == w64)
-    rel = np.where(same_inf, 0.0,
-                   np.abs(g64 - w64) / np.maximum(np.abs(w64), STATE_ATOL_FLOOR))
+    inf = np.isinf(w64) | np.isinf(g64)
+    assert np.array_equal(g64[inf], w64[inf]), f"{what}: infinities differ"
+    g64, w64 = g64[~inf], w64[~inf]
+    rel = np.abs(g64 - w64) / np.maximum(np.abs(w64), STATE_ATOL_FLOOR)
     worst = float(rel.max()) if rel.size else 0.0
     assert worst <= STATE_RTOL, f"{what}: max relative error {worst:.3g} > {STATE_RTOL}"
     return worst
