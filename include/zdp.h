@@ -169,6 +169,30 @@ size_t zdp_step_workspace_bytes(const zdp_step_args* args);
  * caller: do not advance it. */
 int zdp_step(const zdp_step_args* args, void* stream);
 
+/* Largest `len` zdp_step_noalloc accepts (16,777,216 elements). */
+#define ZDP_NOALLOC_MAX_LEN 16777216LL
+
+/* The overflow-checked fused step (zdp_step with check_overflow = 1) for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * to this call; it exists for callers such as a plug-in living inside a
+ * framework whose caching allocator owns the device memory (a raw cudaMalloc
+ * would bypass its accounting, or fail once the pool holds the free memory),
+ * or a step loop that must not call cudaMalloc/cudaFree because they
+ * synchronise the device.
+ *   args  as for zdp_step; check_overflow, workspace and workspace_bytes are
+ *         ignored: the call always runs the two-pass checked step, and its
+ *         scratch is a static device array inside libzdp of 64 MiB + 512 B,
+ *         which every GPU that loads the library holds until the process exits.
+ *   Returns ZDP_ERR_INVALID (nothing enqueued) when args->len exceeds
+ *   ZDP_NOALLOC_MAX_LEN; split longer ranges into several calls.
+ * It calls no allocating routine.  Its first call on a device looks up the
+ * scratch's device address (which may load the library's module on that
+ * device); make that first call before any stream capture.  Every call on a
+ * device uses the same scratch, which keeps the last call's contents (the call
+ * clears the flag itself): calls that may run at the same time on the GPU, e.g.
+ * on two streams without an ordering between them, race on it. */
+int zdp_step_noalloc(const zdp_step_args* args, void* stream);
+
 /* Message for the last non-OK return on this host thread ("" if none). */
 const char* zdp_last_error(void);
 

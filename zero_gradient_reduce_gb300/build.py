@@ -26,7 +26,8 @@ NVCC_FLAGS = [
     "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-ffp-contract=off",
     f"-I{INCLUDE}", f"-I{CSRC}",
 ]
-UNITS = ["zdp_api.cu", "kernels_common.cu", "kernels_bf16.cu", "kernels_fp16.cu"]
+UNITS = ["zdp_api.cu", "kernels_common.cu", "kernels_bf16.cu", "kernels_fp16.cu",
+         "zdp_noalloc.cu"]
 
 
 def nvcc() -> str:

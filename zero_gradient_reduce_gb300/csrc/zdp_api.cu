@@ -102,6 +102,11 @@ bool aligned16(const void* p) { return (addr(p) & 15u) == 0; }
 
 }  // namespace
 
+namespace zdp {
+// Records `msg` as this thread's zdp_last_error() text and returns `code`.
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace zdp
+
 extern "C" {
 
 int zdp_version(void) { return 100; }

@@ -57,6 +57,9 @@ cudaError_t launch_reduce(const KParams& p, int gdt, bool sumsq, bool vec, int n
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
+// Sets this host thread's zdp_last_error() message; returns `code`.
+int report_error(int code, const char* msg);
+
 // Grid size for `kernel` over the elements [p.lo, p.hi): resident blocks per
 // SM (queried once per kernel and cached) times num_sms, capped by the work.
 int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms);

@@ -21,10 +21,12 @@ ZDP_ERR_CUDA = -2
 ZDP_MAX_P = 64
 ZDP_BF16 = 0
 ZDP_FP16 = 1
+ZDP_NOALLOC_MAX_LEN = 16_777_216
 
 EXPORTS = (
     "zdp_version", "zdp_shard_size", "zdp_reduce_scatter", "zdp_adamw_shard",
-    "zdp_all_gather", "zdp_step_workspace_bytes", "zdp_step", "zdp_last_error",
+    "zdp_all_gather", "zdp_step_workspace_bytes", "zdp_step", "zdp_step_noalloc",
+    "zdp_last_error",
 )
 
 
@@ -95,6 +97,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.zdp_step_workspace_bytes.argtypes = [ctypes.POINTER(zdp_step_args)]
     lib.zdp_step.restype = ci
     lib.zdp_step.argtypes = [ctypes.POINTER(zdp_step_args), vp]
+    lib.zdp_step_noalloc.restype = ci
+    lib.zdp_step_noalloc.argtypes = [ctypes.POINTER(zdp_step_args), vp]
     lib.zdp_last_error.restype = ctypes.c_char_p
     lib.zdp_last_error.argtypes = []
     _lib = lib
@@ -219,3 +223,9 @@ def zdp_step_workspace_bytes(args: zdp_step_args) -> int:
 
 def zdp_step(args: zdp_step_args, stream=None) -> None:
     _check(load().zdp_step(ctypes.byref(args), _stream(stream)))
+
+
+def zdp_step_noalloc(args: zdp_step_args, stream=None) -> None:
+    """The overflow-checked step with the library's own static scratch (no
+    workspace, no allocation); len must not exceed ZDP_NOALLOC_MAX_LEN."""
+    _check(load().zdp_step_noalloc(ctypes.byref(args), _stream(stream)))
