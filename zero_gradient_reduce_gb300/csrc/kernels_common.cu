@@ -31,6 +31,9 @@ int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms) {
       resident[kernel] = occ;
     }
   }
+#ifdef ZDP_MAX_BLOCKS_PER_SM
+  if (occ > ZDP_MAX_BLOCKS_PER_SM) occ = ZDP_MAX_BLOCKS_PER_SM;
+#endif
   const int64_t full = static_cast<int64_t>(num_sms) * occ;
   const int64_t need = (work + kThreads - 1) / kThreads;
   return static_cast<int>(need < full ? need : full);

@@ -9,7 +9,10 @@
 
 namespace zdp {
 
-constexpr int kThreads = 256;  // threads per block of every kernel
+#ifndef ZDP_THREADS
+#define ZDP_THREADS 256
+#endif
+constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming kernels
 constexpr int kVec = 8;        // elements per vector: 16 B of bf16, 32 B of fp32
 
 // AdamW constants, prepared once per call on the host.
@@ -44,7 +47,11 @@ struct KParams {
   int32_t* flag;       // nullable: OR-ed with 1 on a non-finite reduced gradient
   double* sumsq;       // nullable: fp64 sum of squares of reduced gradients added
   const int32_t* gate; // nullable: when *gate != 0 the launch writes nothing
+  int32_t* status;     // library status word: ZDP_STATUS_* bits raised by a kernel
 };
+
+// Bits of the library's device status word.
+constexpr int32_t ZDP_STATUS_TIMEOUT = 1;  // a bounded device-side wait gave up
 
 // Launchers, one per kernel family.  `vec` selects the 16-byte-access
 // kernels (every buffer's element 0 on a 16-byte boundary).  The grid is a
