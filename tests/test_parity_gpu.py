@@ -41,7 +41,10 @@ def _compare_step(dev, w, m, v, rep, flag, sumsq, label):
     assert int(dev.flag.item()) == flag, f"{label} flag"
     if sumsq is not None:
         got = float(dev.sumsq.item())
-        assert abs(got - sumsq) <= 1e-9 * abs(sumsq) + 1e-300, (label, got, sumsq)
+        if np.isfinite(sumsq):
+            assert abs(got - sumsq) <= 1e-9 * abs(sumsq) + 1e-300, (label, got, sumsq)
+        else:  # an injected inf gives inf, a NaN (or +inf with -inf) gives NaN
+            assert got == sumsq or (np.isnan(got) and np.isnan(sumsq)), (label, got, sumsq)
 
 
 def _full_case(P, n, seed, gdt=oracle.BF16, t=10, misalign=False, **step_kw):
@@ -241,8 +244,7 @@ def test_fp16_overflow_skip(P):
             ww, mm, vv, rr = w.copy(), m.copy(), v.copy(), rep.copy()
             flag, ss = _oracle_step(gbits, ww, mm, vv, rr, n, scale, 10, oracle.FP16, check=check)
             assert flag == (1 if plan else 0)
-            _compare_step(dev, ww, mm, vv, rr, flag, ss if not plan else None,
-                          f"P={P} case={case} check={check}")
+            _compare_step(dev, ww, mm, vv, rr, flag, ss, f"P={P} case={case} check={check}")
 
 
 def test_checked_step_without_overflow_matches_single_pass():
@@ -270,3 +272,24 @@ def test_finite_gradients_overflowing_fp32():
     flag, _ = _oracle_step(gbits, w, m, v, rep, n, 1.0, 3, check=True)
     assert flag == 1
     _compare_step(dev, w, m, v, rep, 1, None, "fp32 overflow")
+
+
+def test_sum_of_squares_over_extreme_magnitudes():
+    # reduced gradients from 1e-30 to 1e30: squares far outside fp32's range
+    # must still add up like the oracle's fp64 sum
+    P, n = 4, 100_003
+    rng = np.random.default_rng(13)
+    vals = (rng.standard_normal((P, n)) * 10.0 ** rng.uniform(-30, 30, (P, n))).astype(np.float32)
+    gbits = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    dev = DeviceStep(P, n)
+    dev.load(gbits, np.zeros(dev.n_pad), np.zeros(dev.n_pad), np.zeros(dev.n_pad))
+    shards = torch.empty(dev.n_pad, dtype=torch.float32, device="cuda")
+    zdp.zdp_reduce_scatter(dev.grads, shards, n, P, 0.25, dev.flag, dev.sumsq)
+    want, flag, ss = oracle.reduce_scatter(gbits, oracle.BF16, n, 0.25, want_sumsq=True)
+    assert flag == 0 and int(dev.flag.item()) == 0
+    assert np.isfinite(ss) and ss > 1e50
+    assert abs(float(dev.sumsq.item()) - ss) <= 1e-9 * ss
+    # the same through the fused step
+    dev.sumsq.zero_()
+    dev.step(0.25, 3)
+    assert abs(float(dev.sumsq.item()) - ss) <= 1e-9 * ss

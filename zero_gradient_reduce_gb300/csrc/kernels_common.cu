@@ -12,7 +12,7 @@ cudaError_t launch_fused_fp16(const KParams& p, bool sumsq, bool vec, int num_sm
 cudaError_t launch_reduce_bf16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
 cudaError_t launch_reduce_fp16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
 
-int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms) {
+int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms, int cap) {
   const int64_t work = vec ? (p.hi + kVec - 1) / kVec - p.lo / kVec : p.hi - p.lo;
   if (work <= 0) return 0;
   static std::mutex mu;
@@ -31,17 +31,16 @@ int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms) {
       resident[kernel] = occ;
     }
   }
-#ifdef ZDP_MAX_BLOCKS_PER_SM
-  if (occ > ZDP_MAX_BLOCKS_PER_SM) occ = ZDP_MAX_BLOCKS_PER_SM;
-#endif
+  if (occ > cap) occ = cap;
   const int64_t full = static_cast<int64_t>(num_sms) * occ;
   const int64_t need = (work + kThreads - 1) / kThreads;
   return static_cast<int>(need < full ? need : full);
 }
 
 namespace {
-cudaError_t launch_fn(const void* fn, const KParams& p, bool vec, int num_sms, cudaStream_t s) {
-  const int grid = grid_for(fn, p, vec, num_sms);
+cudaError_t launch_fn(const void* fn, const KParams& p, bool vec, int num_sms, int cap,
+                      cudaStream_t s) {
+  const int grid = grid_for(fn, p, vec, num_sms, cap);
   if (grid == 0) return cudaSuccess;
   void* args[] = {const_cast<KParams*>(&p)};
   return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, s);
@@ -63,13 +62,13 @@ cudaError_t launch_reduce(const KParams& p, int gdt, bool sumsq, bool vec, int n
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
   const void* fn = vec ? reinterpret_cast<const void*>(&k_adam_gather<true>)
                        : reinterpret_cast<const void*>(&k_adam_gather<false>);
-  return launch_fn(fn, p, vec, num_sms, s);
+  return launch_fn(fn, p, vec, num_sms, ZDP_CAP_ADAM, s);
 }
 
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
   const void* fn = vec ? reinterpret_cast<const void*>(&k_gather<true>)
                        : reinterpret_cast<const void*>(&k_gather<false>);
-  return launch_fn(fn, p, vec, num_sms, s);
+  return launch_fn(fn, p, vec, num_sms, ZDP_CAP_GATHER, s);
 }
 
 }  // namespace zdp

@@ -10,9 +10,33 @@
 namespace zdp {
 
 #ifndef ZDP_THREADS
-#define ZDP_THREADS 256
+#define ZDP_THREADS 128
 #endif
 constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming kernels
+
+// Resident blocks per SM for each streaming kernel (at most; fewer if the
+// kernel's registers do not allow it).  HBM throughput of these kernels
+// peaks at a moderate number of loads in flight per SM (measured on GB300:
+// 512 threads per SM for P >= 4, 640 for P <= 3, where each thread has fewer
+// bytes in flight); more resident threads lower it again.
+#ifndef ZDP_CAP_FUSED
+#define ZDP_CAP_FUSED 4
+#endif
+#ifndef ZDP_CAP_FUSED_SMALL_P
+#define ZDP_CAP_FUSED_SMALL_P 5
+#endif
+#ifndef ZDP_CAP_REDUCE
+#define ZDP_CAP_REDUCE 12
+#endif
+#ifndef ZDP_CAP_REDUCE_SMALL_P
+#define ZDP_CAP_REDUCE_SMALL_P 5
+#endif
+#ifndef ZDP_CAP_ADAM
+#define ZDP_CAP_ADAM 5
+#endif
+#ifndef ZDP_CAP_GATHER
+#define ZDP_CAP_GATHER 3
+#endif
 constexpr int kVec = 8;        // elements per vector: 16 B of bf16, 32 B of fp32
 
 // AdamW constants, prepared once per call on the host.
@@ -67,8 +91,9 @@ cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t 
 // Sets this host thread's zdp_last_error() message; returns `code`.
 int report_error(int code, const char* msg);
 
-// Grid size for `kernel` over the elements [p.lo, p.hi): resident blocks per
-// SM (queried once per kernel and cached) times num_sms, capped by the work.
-int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms);
+// Grid size for `kernel` over the elements [p.lo, p.hi): min(resident
+// blocks per SM (queried once per kernel and cached), cap) times num_sms,
+// capped by the work.
+int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms, int cap);
 
 }  // namespace zdp

@@ -27,6 +27,10 @@
 
 #include "zdp_internal.h"
 
+#ifndef ZDP_CONTIG
+#define ZDP_CONTIG 0  // 1: block-contiguous spans instead of a grid-wide stride (fused kernel)
+#endif
+
 #ifndef ZDP_SQ_FP64
 #define ZDP_SQ_FP64 0  // 1: accumulate the sum of squares with one fp64 fma per element
 #endif
@@ -291,7 +295,10 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[kVec]) {
 // running sum `hi` with TwoSum (the rounding error is captured exactly),
 // and the small parts collect in `lo`.  Every 32 vectors (<= 256 terms) the
 // pair is flushed into an fp64 total, which bounds the error of the fp32
-// `lo` far below the 1e-9 relative tolerance of the result.
+// `lo` far below the 1e-9 relative tolerance of the result.  Values whose
+// square could leave the range where this split is exact in fp32
+// (|g| outside [2^-40, 2^50), and inf/NaN) go straight to the fp64 total,
+// so an infinite or NaN gradient gives the same inf/NaN as an fp64 sum.
 // ---------------------------------------------------------------------------
 struct SumSq {
   float hi = 0.0f, lo = 0.0f;
@@ -303,6 +310,12 @@ struct SumSq {
     const double d = static_cast<double>(g);
     total = __fma_rn(d, d, total);
 #else
+    const float a = fabsf(g);
+    if (!(a >= 0x1p-40f && a < 0x1p50f)) {  // also taken by NaN
+      const double d = static_cast<double>(g);
+      total = __fma_rn(d, d, total);
+      return;
+    }
     const float p = __fmul_rn(g, g);
     const float e = __fmaf_rn(g, g, -p);
     const float s = __fadd_rn(hi, p);
@@ -406,8 +419,18 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   if constexpr (VEC) {
+#if ZDP_CONTIG
+    // each block walks its own contiguous span of vectors
+    const int64_t nv = (p.hi + kVec - 1) / kVec - p.lo / kVec;
+    const int64_t span = (nv + gridDim.x - 1) / gridDim.x;
+    const int64_t vlo = p.lo / kVec + static_cast<int64_t>(blockIdx.x) * span;
+    const int64_t vend = (p.hi + kVec - 1) / kVec;
+    const int64_t vhi = vlo + span < vend ? vlo + span : vend;
+    for (int64_t vi = vlo + threadIdx.x; vi < vhi; vi += kThreads) {
+#else
     const int64_t vlo = p.lo / kVec, vhi = (p.hi + kVec - 1) / kVec;
     for (int64_t vi = vlo + tid; vi < vhi; vi += stride) {
+#endif
       const int64_t i0 = vi * kVec;
       const int r = owner_of(i0, p, P);
       if (i0 >= p.lo && i0 + kVec <= p.hi && i0 + kVec <= static_cast<int64_t>(r + 1) * p.S) {
