@@ -7,10 +7,10 @@
 
 namespace zdp {
 
-cudaError_t launch_fused_bf16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
-cudaError_t launch_fused_fp16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
-cudaError_t launch_reduce_bf16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
-cudaError_t launch_reduce_fp16(const KParams& p, bool sumsq, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_fused_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_fused_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_reduce_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_reduce_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
 int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms, int cap) {
   const int64_t work = vec ? (p.hi + kVec - 1) / kVec - p.lo / kVec : p.hi - p.lo;
@@ -47,22 +47,20 @@ cudaError_t launch_fn(const void* fn, const KParams& p, bool vec, int num_sms, i
 }
 }  // namespace
 
-cudaError_t launch_fused(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
-                         cudaStream_t s) {
-  return gdt == ZDP_BF16 ? launch_fused_bf16(p, sumsq, vec, num_sms, s)
-                         : launch_fused_fp16(p, sumsq, vec, num_sms, s);
+cudaError_t launch_fused(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s) {
+  return gdt == ZDP_BF16 ? launch_fused_bf16(p, vec, num_sms, s)
+                         : launch_fused_fp16(p, vec, num_sms, s);
 }
 
-cudaError_t launch_reduce(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
-                          cudaStream_t s) {
-  return gdt == ZDP_BF16 ? launch_reduce_bf16(p, sumsq, vec, num_sms, s)
-                         : launch_reduce_fp16(p, sumsq, vec, num_sms, s);
+cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s) {
+  return gdt == ZDP_BF16 ? launch_reduce_bf16(p, vec, num_sms, s)
+                         : launch_reduce_fp16(p, vec, num_sms, s);
 }
 
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
   const void* fn = vec ? reinterpret_cast<const void*>(&k_adam_gather<true>)
                        : reinterpret_cast<const void*>(&k_adam_gather<false>);
-  return launch_fn(fn, p, vec, num_sms, ZDP_CAP_ADAM, s);
+  return launch_fn(fn, p, vec, num_sms, p.nrep > 0 ? ZDP_CAP_ADAM_GATHER : ZDP_CAP_ADAM, s);
 }
 
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {

@@ -166,7 +166,7 @@ int zdp_reduce_scatter(const void* const* grads, int gdt, float* shards, int64_t
   p.flag = d_overflow;
   p.sumsq = d_sumsq;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = zdp::launch_reduce(p, gdt, d_sumsq != nullptr, vec, sms, s);
+  cudaError_t e = zdp::launch_reduce(p, gdt, vec, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter launch");
   if (P * S > n) {
     e = cudaMemsetAsync(shards + n, 0, static_cast<size_t>(P * S - n) * 4, s);
@@ -328,7 +328,6 @@ int zdp_step(const zdp_step_args* a, void* stream) {
   p.scale = a->scale;
   p.ad = make_adam(a->lr, a->b1, a->b2, a->eps, a->wd, a->t);
   const int64_t bucket = a->bucket_elems > 0 ? a->bucket_elems : len;
-  const bool sq = a->d_sumsq != nullptr;
 
   if (!a->check_overflow) {
     p.flag = a->d_overflow;
@@ -336,7 +335,7 @@ int zdp_step(const zdp_step_args* a, void* stream) {
     for (int64_t lo = off; lo < off + len; lo += bucket) {
       p.lo = lo;
       p.hi = std::min(off + len, lo + bucket);
-      cudaError_t e = zdp::launch_fused(p, a->gdt, sq, vec, sms, s);
+      cudaError_t e = zdp::launch_fused(p, a->gdt, vec, sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "fused step launch");
     }
     return ok();
@@ -355,7 +354,7 @@ int zdp_step(const zdp_step_args* a, void* stream) {
   for (int64_t lo = off; lo < off + len; lo += bucket) {
     p.lo = lo;
     p.hi = std::min(off + len, lo + bucket);
-    e = zdp::launch_reduce(p, a->gdt, sq, vec, sms, s);
+    e = zdp::launch_reduce(p, a->gdt, vec, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "reduce pass launch");
   }
   p.gout = nullptr;

@@ -16,9 +16,12 @@ constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming ker
 
 // Resident blocks per SM for each streaming kernel (at most; fewer if the
 // kernel's registers do not allow it).  HBM throughput of these kernels
-// peaks at a moderate number of loads in flight per SM (measured on GB300:
-// 512 threads per SM for P >= 4, 640 for P <= 3, where each thread has fewer
-// bytes in flight); more resident threads lower it again.
+// peaks at a moderate number of loads in flight per SM and falls again when
+// more threads are resident; the caps are the measured optima on GB300
+// (fused step: 512 threads per SM for P >= 4, 640 for P <= 3, where each
+// thread has fewer bytes in flight; reduce-scatter, which keeps only its
+// gradient loads in flight, 1536 and 1024; AdamW 640; AdamW with the replica
+// stores 512; all-gather 384).
 #ifndef ZDP_CAP_FUSED
 #define ZDP_CAP_FUSED 4
 #endif
@@ -29,10 +32,13 @@ constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming ker
 #define ZDP_CAP_REDUCE 12
 #endif
 #ifndef ZDP_CAP_REDUCE_SMALL_P
-#define ZDP_CAP_REDUCE_SMALL_P 5
+#define ZDP_CAP_REDUCE_SMALL_P 8
 #endif
 #ifndef ZDP_CAP_ADAM
 #define ZDP_CAP_ADAM 5
+#endif
+#ifndef ZDP_CAP_ADAM_GATHER
+#define ZDP_CAP_ADAM_GATHER 4
 #endif
 #ifndef ZDP_CAP_GATHER
 #define ZDP_CAP_GATHER 3
@@ -71,20 +77,15 @@ struct KParams {
   int32_t* flag;       // nullable: OR-ed with 1 on a non-finite reduced gradient
   double* sumsq;       // nullable: fp64 sum of squares of reduced gradients added
   const int32_t* gate; // nullable: when *gate != 0 the launch writes nothing
-  int32_t* status;     // library status word: ZDP_STATUS_* bits raised by a kernel
 };
-
-// Bits of the library's device status word.
-constexpr int32_t ZDP_STATUS_TIMEOUT = 1;  // a bounded device-side wait gave up
 
 // Launchers, one per kernel family.  `vec` selects the 16-byte-access
 // kernels (every buffer's element 0 on a 16-byte boundary).  The grid is a
 // persistent grid-stride grid: `num_sms` times the kernel's resident blocks
 // per SM, capped by the work.  Each returns the launch status.
-cudaError_t launch_fused(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
-                         cudaStream_t s);
-cudaError_t launch_reduce(const KParams& p, int gdt, bool sumsq, bool vec, int num_sms,
-                          cudaStream_t s);
+// The fused and reduce kernels add the sum of squares when p.sumsq is set.
+cudaError_t launch_fused(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s);
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
