@@ -47,7 +47,8 @@ METRIC = "ZeRO step params/s and achieved HBM TB/s vs roofline (1.3B params, P=8
 HP = dict(lr=1e-4, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("zero_gradient_reduce_gb300/csrc/zdp_kernels.cuh",
-                  "zero_gradient_reduce_gb300/csrc/kernels_grad.inc")
+                  "zero_gradient_reduce_gb300/csrc/kernels_grad.inc",
+                  "zero_gradient_reduce_gb300/csrc/zdp_internal.h")
 
 
 def parse_args():
@@ -66,12 +67,31 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=1 << 24,
                     help="parameters per oracle step in the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="fp16 overflow-checked step over n = 1K..256M and P = 2..64: one "
+                         "JSON line per point (cold and warm L2) instead of the benchmark line")
     return ap.parse_args()
 
 
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(units_per_rank: int, steps: int, world: int, slowest_ms: float) -> float:
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return world * units_per_rank * steps / (slowest_ms / 1e3)
 
 
 def bytes_per_param(P: int) -> int:
@@ -290,23 +310,17 @@ def run_ours(args):
     elapsed_ms = start.elapsed_time(end)
     kernel_ms = sum(ev0[k].elapsed_time(ev1[k]) for k in range(K)) / K
     step_flag = int(flag.item())
-    times = torch.tensor([elapsed_ms, kernel_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, kernel_ms = float(times[0]), float(times[1])
+    elapsed_ms, kernel_ms = max_over_ranks([elapsed_ms, kernel_ms], dev)
     ms_per_step = elapsed_ms / K
-    value = world * n * K / (elapsed_ms / 1e3)
+    value = whole_job_rate(n, K, world, elapsed_ms)
 
     # ---- end to end through the C ABI: gradients from pinned host memory
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t)
-        if world > 1:
-            x = torch.tensor([e2e.get("seconds_per_step") or 0.0], dtype=torch.float64,
-                             device=dev)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            if e2e.get("value") is not None:
-                e2e["value"] = world * n / float(x[0])
+        slowest = max_over_ranks([e2e.get("seconds_per_step") or 0.0], dev)[0]
+        if e2e.get("value") is not None:
+            e2e["value"] = whole_job_rate(n, 1, world, slowest * 1e3)
         e2e.pop("seconds_per_step", None)
 
     out = None
@@ -360,9 +374,15 @@ def run_ours(args):
 
 
 def run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t0):
-    """Gradients copied host->device every step (bucket by bucket on a copy
-    stream, overlapped with zdp_step on the previous bucket), flag and sum of
-    squares read back to the host; wall clock over whole steps."""
+    """End to end through the C ABI with the gradients in pinned host memory.
+
+    Primary (`value`): the step's kernel reads the P gradient buffers straight
+    from pinned host memory over the host link (GB300's host memory is mapped
+    into the GPU's address space), so the step needs no staging copy; the
+    flag and sum of squares are read back to the host every step.  Secondary
+    (`memcpy_pipeline_value`): the gradients are copied host->device bucket by
+    bucket on a copy stream, each bucket's zdp_step overlapped with the next
+    bucket's copy.  Both are wall-clock times over whole steps."""
     import torch
 
     from zero_gradient_reduce_gb300 import zdp
@@ -375,19 +395,33 @@ def run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t0
     for q in range(P):
         host[q].copy_(grads[q])
     host_words = torch.empty(16, dtype=torch.uint8, pin_memory=True)
-    B = max(1, args.e2e_bucket)
-    bounds = [(lo, min(n, lo + B)) for lo in range(0, n, B)]
-    argv = []
-    for lo, hi in bounds:
-        a, keep = zdp.make_step_args([g[lo:hi] for g in grads], master, m, v, replicas, n=n,
-                                     scale=wl.scale, t=1, off=lo, length=hi - lo,
-                                     d_overflow=flag, d_sumsq=sumsq, **HP)
-        argv.append((a, keep))
     main = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
+    K = max(1, args.e2e_steps)
     t = t0
 
-    def step():
+    # zero-copy: one zdp_step whose gradient pointers are the pinned host buffers
+    a0, keep0 = zdp.make_step_args(host, master, m, v, replicas, n=n, scale=wl.scale, t=1,
+                                   d_overflow=flag, d_sumsq=sumsq, **HP)
+
+    def step_zero_copy():
+        nonlocal t
+        t += 1
+        words.zero_()
+        a0.t = t
+        zdp.zdp_step(a0, main)
+        host_words.copy_(words, non_blocking=True)
+        main.synchronize()
+        return int(host_words[0:4].view(torch.int32)[0])
+
+    # memcpy pipeline
+    B = max(1, args.e2e_bucket)
+    bounds = [(lo, min(n, lo + B)) for lo in range(0, n, B)]
+    argv = [zdp.make_step_args([g[lo:hi] for g in grads], master, m, v, replicas, n=n,
+                               scale=wl.scale, t=1, off=lo, length=hi - lo, d_overflow=flag,
+                               d_sumsq=sumsq, **HP) for lo, hi in bounds]
+    copy = torch.cuda.Stream(dev)
+
+    def step_memcpy():
         nonlocal t
         t += 1
         words.zero_()
@@ -406,15 +440,23 @@ def run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t0
         main.synchronize()
         return int(host_words[0:4].view(torch.int32)[0])
 
-    step()  # warm-up
-    K = max(1, args.e2e_steps)
-    t_start = time.perf_counter()
-    for _ in range(K):
-        step()
-    secs = (time.perf_counter() - t_start) / K
+    def timed(fn):
+        fn()  # warm-up
+        t_start = time.perf_counter()
+        for _ in range(K):
+            fn()
+        return (time.perf_counter() - t_start) / K
+
+    secs = timed(step_zero_copy)
+    secs_memcpy = timed(step_memcpy)
     return {"value": n / secs, "unit": "params/s", "h2d_bytes_per_step": 2 * P * n,
-            "d2h_bytes_per_step": 16, "steps": K, "bucket_elems": B,
-            "gpu_launches_per_step": len(bounds), "seconds_per_step": secs}
+            "d2h_bytes_per_step": 16, "steps": K,
+            "method": "zdp_step reads the gradients from pinned host memory (no staging copy)",
+            "gpu_launches_per_step": 1,
+            "host_link_GBps": 2 * P * n / secs / 1e9,
+            "memcpy_pipeline_value": n / secs_memcpy,
+            "memcpy_pipeline_bucket_elems": B,
+            "seconds_per_step": secs}
 
 
 def _oracle_slice(P, S, n, length):
@@ -516,10 +558,80 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_sweep(args):
+    """GB/s of the overflow-checked step (two passes: reduced gradients to the
+    workspace, then the flag-gated AdamW + all-gather) against n and P, fp16
+    gradients scaled by 2^16.  Cold: the L2 is flushed (a write of twice its
+    size) before every timed step; warm: steps back to back.  Bytes per step
+    are (2P + 4) n for the first pass and (4 + 24 + 2P) n for the second."""
+    import torch
+
+    from zero_gradient_reduce_gb300 import workloads, zdp
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    zdp.load()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(3, min(args.steps, 20))
+    for P in workloads.SWEEP_P:
+        for n in workloads.SWEEP_N:
+            wl = workloads.sweep_point(n, P)
+            S = -(-n // P)
+            grads = [torch.empty(n, dtype=torch.float16, device=dev) for _ in range(P)]
+            for q in range(P):
+                workloads.fill_grads(grads[q], wl, q, 0, args.seed)
+            st = [torch.empty(P * S, dtype=torch.float32, device=dev) for _ in range(3)]
+            workloads.fill_state(st[0], st[1], st[2], wl, args.seed)
+            reps_buf = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+            words = torch.zeros(16, dtype=torch.uint8, device=dev)
+            a, keep = zdp.make_step_args(grads, st[0], st[1], st[2], reps_buf, n=n,
+                                         scale=wl.scale, t=1, check_overflow=True,
+                                         d_overflow=words[0:4].view(torch.int32), **HP)
+            ws = torch.empty(zdp.zdp_step_workspace_bytes(a), dtype=torch.uint8, device=dev)
+            a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+            t = 0
+
+            def one(e0=None, e1=None):
+                nonlocal t
+                t += 1
+                a.t = t
+                if e0 is not None:
+                    e0.record(stream)
+                zdp.zdp_step(a, stream)
+                if e1 is not None:
+                    e1.record(stream)
+
+            for _ in range(args.warmup):
+                one()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(2 * reps)]
+            for k in range(reps):  # cold
+                flush.zero_()
+                one(*ev[k])
+            for k in range(reps, 2 * reps):  # warm
+                one(*ev[k])
+            torch.cuda.synchronize()
+            cold = sorted(e0.elapsed_time(e1) for e0, e1 in ev[:reps])[reps // 2]
+            warm = sorted(e0.elapsed_time(e1) for e0, e1 in ev[reps:])[reps // 2]
+            nbytes = (4 * P + 32) * n
+            print(json.dumps({"sweep": "fp16_checked_step", "P": P, "n": n,
+                              "us_cold": cold * 1e3, "us_warm": warm * 1e3,
+                              "GBps_cold": nbytes / cold / 1e6, "GBps_warm": nbytes / warm / 1e6,
+                              "bytes_per_step": nbytes, "launches_per_step": 2,
+                              "overflow_flag": int(words[0:4].view(torch.int32).item())}),
+                  flush=True)
+            del grads, st, reps_buf, ws, keep
+            torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 
