@@ -67,6 +67,9 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=1 << 24,
                     help="parameters per oracle step in the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ring-study", action="store_true",
+                    help="fused step against the literal ring schedule (zdp_step_ring) for "
+                         "P = 2..64: one JSON line per P")
     ap.add_argument("--sweep", action="store_true",
                     help="fp16 overflow-checked step over n = 1K..256M and P = 2..64: one "
                          "JSON line per point (cold and warm L2) instead of the benchmark line")
@@ -708,12 +711,75 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+def run_ring_study(args):
+    """The same step as one fused pass (zdp_step) and as the literal ring
+    schedule (zdp_step_ring: P-1 reduce-scatter launches passing fp32 partial
+    sums, the owner's update, P-1 all-gather launches), bf16 gradients, inputs
+    resident, median of `steps` CUDA-event timings each.  busbw follows the
+    nccl-tests definition for an all-reduce of the n-element bf16 gradient:
+    algbw = 2n bytes / time, busbw = algbw * 2(P-1)/P."""
+    import torch
+
+    from zero_gradient_reduce_gb300 import workloads, zdp
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    zdp.load()
+    stream = torch.cuda.current_stream(dev)
+    for P in (2, 4, 8, 16, 64):
+        n = (1 << 28) if P <= 16 else (1 << 26)
+        wl = workloads.Workload(f"flat_{n}_p{P}", P=P, n=n, tensors=workloads._flat(n),
+                                fresh_state=True)
+        S = -(-n // P)
+        grads = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        for q in range(P):
+            workloads.fill_grads(grads[q], wl, q, 0, args.seed)
+        st = [torch.zeros(P * S, dtype=torch.float32, device=dev) for _ in range(3)]
+        workloads.fill_state(st[0], st[1], st[2], wl, args.seed)
+        reps = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        a, keep = zdp.make_step_args(grads, st[0], st[1], st[2], reps, n=n, scale=wl.scale, t=1,
+                                     **HP)
+        ws = torch.empty(zdp.zdp_step_ring_workspace_bytes(a), dtype=torch.uint8, device=dev)
+        res = {}
+        for name, fn in (("fused", zdp.zdp_step), ("ring", zdp.zdp_step_ring)):
+            if name == "ring":
+                a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+            ms = []
+            for k in range(args.warmup + args.steps):
+                a.t = k + 1
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn(a, stream)
+                e1.record(stream)
+                e1.synchronize()
+                if k >= args.warmup:
+                    ms.append(e0.elapsed_time(e1))
+            res[name] = sorted(ms)[len(ms) // 2]
+        fused_b, ring_b = (4 * P + 24) * n, (14 * P + 14) * n
+        algbw = lambda t: 2 * n / (t / 1e3) / 1e9
+        print(json.dumps({
+            "ring_study": "bf16 step", "P": P, "n": n,
+            "fused_ms": res["fused"], "ring_ms": res["ring"],
+            "ring_over_fused": res["ring"] / res["fused"],
+            "fused_launches": 1, "ring_launches": 2 * P - 1,
+            "fused_bytes": fused_b, "ring_bytes": ring_b,
+            "fused_TBps": fused_b / (res["fused"] / 1e3) / 1e12,
+            "ring_TBps": ring_b / (res["ring"] / 1e3) / 1e12,
+            "fused_busbw_GBps": algbw(res["fused"]) * 2 * (P - 1) / P,
+            "ring_busbw_GBps": algbw(res["ring"]) * 2 * (P - 1) / P,
+        }), flush=True)
+        del grads, st, reps, ws, keep
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.ring_study:
+        run_ring_study(args)
     else:
         run_ours(args)
 

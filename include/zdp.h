@@ -169,6 +169,26 @@ size_t zdp_step_workspace_bytes(const zdp_step_args* args);
  * caller: do not advance it. */
 int zdp_step(const zdp_step_args* args, void* stream);
 
+/* The same step as zdp_step, run as the literal ring schedule of the pages
+ * instead of one fused pass, for measuring what the fused pass saves.
+ * Reduce-scatter: P-1 launches; at step s every rank i adds its own chunk
+ * (i-s-1) mod P to the fp32 partial sum received from rank i-1 (Fudan MLSys
+ * ch. 9, 9.3.6; CS336 Lecture 7 notes 4.2, in the labelling where rank r
+ * finishes chunk r).  Then one launch: the owner's last add, scale, AdamW and
+ * the bf16 write of the owner's chunk of its own replica.  All-gather: P-1
+ * launches, step s copying chunk (i-s) mod P of replica i into replica i+1.
+ * The partial sums travel through `workspace` (2*P*S fp32 "messages",
+ * zdp_step_ring_workspace_bytes(args) bytes, 16-byte aligned).
+ * Results are bit-identical to zdp_step (same additions in the same order).
+ * The call covers the whole model: off = 0, len = n, bucket_elems = 0 and
+ * check_overflow = 0 are required (ZDP_ERR_INVALID otherwise); d_overflow and
+ * d_sumsq work as for zdp_step.  With bf16 gradients it moves about
+ * (14P + 14) bytes of HBM traffic per parameter (each of the P-2 middle
+ * reduce-scatter steps reads and writes the fp32 messages), against
+ * (4P + 24) for zdp_step. */
+size_t zdp_step_ring_workspace_bytes(const zdp_step_args* args);
+int zdp_step_ring(const zdp_step_args* args, void* stream);
+
 /* Largest `len` zdp_step_noalloc accepts (16,777,216 elements). */
 #define ZDP_NOALLOC_MAX_LEN 16777216LL
 

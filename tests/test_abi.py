@@ -120,3 +120,22 @@ def test_unfused_calls_reject_bad_arguments(lib):
 def test_zero_length_step_is_a_host_no_op(lib):
     a, keep = _args(off=10, length=0)
     zdp.zdp_step(a, stream=0)
+
+
+@pytest.mark.parametrize("mutate,needle", [
+    (lambda a: setattr(a, "off", 1), "whole model"),
+    (lambda a: setattr(a, "len", 10), "whole model"),
+    (lambda a: setattr(a, "check_overflow", 1), "overflow"),
+    (lambda a: setattr(a, "bucket_elems", 64), "buckets"),
+    (lambda a: None, "workspace"),  # no workspace given
+])
+def test_ring_rejects_bad_arguments(lib, mutate, needle):
+    a, keep = _args()
+    mutate(a)
+    with pytest.raises(zdp.ZdpError, match=needle):
+        zdp.zdp_step_ring(a, stream=0)
+
+
+def test_ring_workspace_bytes(lib):
+    a, keep = _args()  # n = 1000, P = 2: S = 500, two message sets of P*S fp32
+    assert zdp.zdp_step_ring_workspace_bytes(a) == (2 * 2 * 500 * 4 + 255) // 256 * 256

@@ -249,7 +249,14 @@ size_t zdp_step_workspace_bytes(const zdp_step_args* a) {
   return 256 + ((body + 255) / 256) * 256;
 }
 
-int zdp_step(const zdp_step_args* a, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks of zdp_step / zdp_step_ring arguments; `ws_need` is the workspace the
+// call needs (0: none).  Sets *vec when every buffer's element 0 is 16-byte
+// aligned.  Returns ZDP_OK, or ZDP_ERR_INVALID with the message set.
+int validate_step(const zdp_step_args* a, size_t ws_need, bool* vec_out) {
   if (!a) return fail(ZDP_ERR_INVALID, "args is NULL");
   const int P = a->P;
   if (!valid_p(P)) return fail(ZDP_ERR_INVALID, "P=%d outside 1..%d", P, ZDP_MAX_P);
@@ -264,7 +271,6 @@ int zdp_step(const zdp_step_args* a, void* stream) {
   if (a->bucket_elems < 0) return fail(ZDP_ERR_INVALID, "bucket_elems < 0");
   if (!a->grads || !a->replicas) return fail(ZDP_ERR_INVALID, "grads or replicas is NULL");
   if (!a->master || !a->m || !a->v) return fail(ZDP_ERR_INVALID, "master, m or v is NULL");
-  if (a->len == 0) return ok();
   const int64_t n = a->n, off = a->off, len = a->len;
   const float* st[3] = {a->master, a->m, a->v};
   bool vec = true;
@@ -290,9 +296,8 @@ int zdp_step(const zdp_step_args* a, void* stream) {
   }
   add_range(outs, a->d_overflow, 4, "d_overflow", 0);
   add_range(outs, a->d_sumsq, 8, "d_sumsq", 0);
-  const size_t ws_need = zdp_step_workspace_bytes(a);
-  if (a->check_overflow) {
-    if (!a->workspace) return fail(ZDP_ERR_INVALID, "check_overflow needs a workspace");
+  if (ws_need > 0) {
+    if (!a->workspace) return fail(ZDP_ERR_INVALID, "this call needs a workspace");
     if (a->workspace_bytes < ws_need)
       return fail(ZDP_ERR_INVALID, "workspace of %zu bytes, need %zu", a->workspace_bytes, ws_need);
     if (!aligned16(a->workspace)) return fail(ZDP_ERR_INVALID, "workspace not 16-byte aligned");
@@ -305,7 +310,23 @@ int zdp_step(const zdp_step_args* a, void* stream) {
       if (lo < o.hi && o.lo < hi)
         return fail(ZDP_ERR_INVALID, "buffers overlap: grads[%d] and %s[%d]", q, o.what, o.index);
   }
+  *vec_out = vec;
+  return ZDP_OK;
+}
 
+}  // namespace
+
+extern "C" {
+
+int zdp_step(const zdp_step_args* a, void* stream) {
+  if (a && a->len == 0 && a->P >= 1 && a->P <= ZDP_MAX_P && a->n >= 1 && a->off >= 0 &&
+      a->off <= a->n && a->t >= 1 && a->grads && a->replicas && a->master && a->m && a->v &&
+      (a->gdt == ZDP_BF16 || a->gdt == ZDP_FP16) && a->bucket_elems >= 0)
+    return ok();
+  bool vec = false;
+  if (validate_step(a, zdp_step_workspace_bytes(a), &vec) != ZDP_OK) return ZDP_ERR_INVALID;
+  const int P = a->P;
+  const int64_t n = a->n, off = a->off, len = a->len;
   int sms = 0;
   if (num_sms(&sms) != ZDP_OK) return ZDP_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -369,6 +390,29 @@ int zdp_step(const zdp_step_args* a, void* stream) {
     e = zdp::launch_adam_gather(p, vec, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "update pass launch");
   }
+  return ok();
+}
+
+size_t zdp_step_ring_workspace_bytes(const zdp_step_args* a) {
+  if (!a || !valid_p(a->P) || a->n < 1) return 0;
+  const size_t msgs = 2u * static_cast<size_t>(a->P) * static_cast<size_t>(shard(a->n, a->P)) * 4u;
+  return (msgs + 255) / 256 * 256;
+}
+
+int zdp_step_ring(const zdp_step_args* a, void* stream) {
+  if (!a) return fail(ZDP_ERR_INVALID, "args is NULL");
+  if (a->off != 0 || a->len != a->n)
+    return fail(ZDP_ERR_INVALID, "the ring schedule covers the whole model: off = 0, len = n");
+  if (a->check_overflow) return fail(ZDP_ERR_INVALID, "zdp_step_ring has no overflow check");
+  if (a->bucket_elems != 0) return fail(ZDP_ERR_INVALID, "zdp_step_ring takes no buckets");
+  bool vec = false;
+  if (validate_step(a, zdp_step_ring_workspace_bytes(a), &vec) != ZDP_OK) return ZDP_ERR_INVALID;
+  int sms = 0;
+  if (num_sms(&sms) != ZDP_OK) return ZDP_ERR_CUDA;
+  const zdp::AdamK ad = make_adam(a->lr, a->b1, a->b2, a->eps, a->wd, a->t);
+  cudaError_t e = zdp::launch_ring(a, ad, static_cast<float*>(a->workspace), vec, sms,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ring step launch");
   return ok();
 }
 

@@ -89,6 +89,11 @@ cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cuda
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
+// The literal ring schedule of zdp_step_ring (zdp_ring.cu); `ws` holds the
+// 2 * P * S fp32 messages.
+cudaError_t launch_ring(const zdp_step_args* a, const AdamK& ad, float* ws, bool vec, int num_sms,
+                        cudaStream_t s);
+
 // Sets this host thread's zdp_last_error() message; returns `code`.
 int report_error(int code, const char* msg);
 

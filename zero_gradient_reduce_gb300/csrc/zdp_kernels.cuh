@@ -333,11 +333,12 @@ __device__ __forceinline__ void account1(float g, bool sq, bool& bad, SumSq& ss)
   }
 }
 
-__device__ __forceinline__ void publish(const KParams& p, bool bad, SumSq& acc) {
+// Block-level OR of the flag and sum of the squares into the caller's words.
+__device__ __forceinline__ void publish_to(int32_t* flag, double* sumsq, bool bad, SumSq& acc) {
   // Every thread of the block reaches this point exactly once.
   const int any_bad = __syncthreads_or(bad ? 1 : 0);
-  if (threadIdx.x == 0 && any_bad && p.flag) atomicOr(p.flag, 1);
-  if (p.sumsq) {
+  if (threadIdx.x == 0 && any_bad && flag) atomicOr(flag, 1);
+  if (sumsq) {
     double ss = acc.value();
     __shared__ double part[kThreads / 32];
 #pragma unroll
@@ -348,9 +349,13 @@ __device__ __forceinline__ void publish(const KParams& p, bool bad, SumSq& acc) 
       double t = 0.0;
 #pragma unroll
       for (int k = 0; k < kThreads / 32; ++k) t += part[k];
-      atomicAdd(p.sumsq, t);
+      atomicAdd(sumsq, t);
     }
   }
+}
+
+__device__ __forceinline__ void publish(const KParams& p, bool bad, SumSq& acc) {
+  publish_to(p.flag, p.sumsq, bad, acc);
 }
 
 // ---------------------------------------------------------------------------

@@ -26,7 +26,7 @@ ZDP_NOALLOC_MAX_LEN = 16_777_216
 EXPORTS = (
     "zdp_version", "zdp_shard_size", "zdp_reduce_scatter", "zdp_adamw_shard",
     "zdp_all_gather", "zdp_step_workspace_bytes", "zdp_step", "zdp_step_noalloc",
-    "zdp_last_error",
+    "zdp_step_ring_workspace_bytes", "zdp_step_ring", "zdp_last_error",
 )
 
 
@@ -97,6 +97,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.zdp_step_workspace_bytes.argtypes = [ctypes.POINTER(zdp_step_args)]
     lib.zdp_step.restype = ci
     lib.zdp_step.argtypes = [ctypes.POINTER(zdp_step_args), vp]
+    lib.zdp_step_ring_workspace_bytes.restype = ctypes.c_size_t
+    lib.zdp_step_ring_workspace_bytes.argtypes = [ctypes.POINTER(zdp_step_args)]
+    lib.zdp_step_ring.restype = ci
+    lib.zdp_step_ring.argtypes = [ctypes.POINTER(zdp_step_args), vp]
     lib.zdp_step_noalloc.restype = ci
     lib.zdp_step_noalloc.argtypes = [ctypes.POINTER(zdp_step_args), vp]
     lib.zdp_last_error.restype = ctypes.c_char_p
@@ -223,6 +227,16 @@ def zdp_step_workspace_bytes(args: zdp_step_args) -> int:
 
 def zdp_step(args: zdp_step_args, stream=None) -> None:
     _check(load().zdp_step(ctypes.byref(args), _stream(stream)))
+
+
+def zdp_step_ring_workspace_bytes(args: zdp_step_args) -> int:
+    return int(load().zdp_step_ring_workspace_bytes(ctypes.byref(args)))
+
+
+def zdp_step_ring(args: zdp_step_args, stream=None) -> None:
+    """The step as the literal ring schedule (2P-1 launches); args.workspace
+    must hold zdp_step_ring_workspace_bytes(args) bytes."""
+    _check(load().zdp_step_ring(ctypes.byref(args), _stream(stream)))
 
 
 def zdp_step_noalloc(args: zdp_step_args, stream=None) -> None:
