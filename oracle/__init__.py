@@ -71,6 +71,13 @@ def _load():
             "ora_step_sampled": (ctypes.c_int, [vp, vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, i64,
                                                 ctypes.c_int, f32, f32, f32, f32, f32, f32,
                                                 ctypes.c_int, ctypes.c_int, vp]),
+            "ora_step_mdt": (ctypes.c_int, [vp, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp,
+                                            i64, i64, i64, i64, i64, ctypes.c_int, f32, f32, f32,
+                                            f32, f32, f32, ctypes.c_int, ctypes.c_int, vp, vp]),
+            "ora_step_sampled_mdt": (ctypes.c_int, [vp, vp, i64, ctypes.c_int, vp, vp, vp,
+                                                    ctypes.c_int, vp, vp, i64, ctypes.c_int, f32,
+                                                    f32, f32, f32, f32, f32, ctypes.c_int,
+                                                    ctypes.c_int, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -180,51 +187,62 @@ def all_gather(master, n: int, P: int) -> np.ndarray:
     return rep
 
 
+MOMENTS = {"f32": (0, np.float32), "bf16": (1, np.uint16)}
+
+
 def step(grads, gdt, master, m, v, replicas, n, off, len_, scale, lr, b1, b2, eps, wd, t,
-         check_overflow=False, base=0):
+         check_overflow=False, base=0, moments="f32"):
     """The fused step on host arrays, in place on master/m/v/replicas.
 
     grads: [P, >=len_] uint16 rows holding elements [off, off+len_).
-    master/m/v: float32 arrays holding global elements [base, off+len_).
+    master: float32 array holding global elements [base, off+len_); m and v
+    likewise, float32 (moments="f32") or bf16 bit patterns as uint16
+    (moments="bf16").
     replicas: [P, >= off+len_-base] uint16, element i in column i - base.
     Returns (overflow, sumsq).
     """
     g = _gbits(grads)
     P = g.shape[0]
+    mdt, mtype = MOMENTS[moments]
     assert 0 <= base <= off
     need = off + len_ - base
-    for a in (master, m, v):
-        assert a.dtype == np.float32 and a.flags.c_contiguous and a.size >= need
+    assert master.dtype == np.float32 and master.flags.c_contiguous and master.size >= need
+    for a in (m, v):
+        assert a.dtype == mtype and a.flags.c_contiguous and a.size >= need
     assert replicas.dtype == np.uint16 and replicas.flags.c_contiguous
     assert replicas.shape[0] == P and replicas.shape[1] >= need
     flag = np.zeros(1, np.int32)
     ss = np.zeros(1, np.float64)
-    rc = _load().ora_step(_ptr(g), g.shape[1], gdt, _ptr(master), _ptr(m), _ptr(v),
-                          _ptr(replicas), replicas.shape[1], base, n, off, len_, P, scale, lr,
-                          b1, b2, eps, wd, t, int(bool(check_overflow)), _ptr(flag), _ptr(ss))
+    rc = _load().ora_step_mdt(_ptr(g), g.shape[1], gdt, _ptr(master), _ptr(m), _ptr(v), mdt,
+                              _ptr(replicas), replicas.shape[1], base, n, off, len_, P, scale, lr,
+                              b1, b2, eps, wd, t, int(bool(check_overflow)), _ptr(flag), _ptr(ss))
     if rc != 0:
         raise ValueError("oracle step: bad arguments")
     return int(flag[0]), float(ss[0])
 
 
-def step_sampled(gs, idx, gdt, w, m, v, n, scale, lr, b1, b2, eps, wd, t, skip=False):
+def step_sampled(gs, idx, gdt, w, m, v, n, scale, lr, b1, b2, eps, wd, t, skip=False,
+                 moments="f32"):
     """The step on k sampled global indices.
 
-    gs: [P, k] uint16 gradient values at idx; w/m/v: [k] float32 (updated in
-    place).  Returns (g_reduced[k] fp32, replica_bits[k] uint16, overflow).
+    gs: [P, k] uint16 gradient values at idx; w: [k] float32, m/v: [k]
+    float32 or bf16 bits (moments="bf16"), all updated in place.  Returns
+    (g_reduced[k] fp32, replica_bits[k] uint16, overflow).
     """
     g = _gbits(gs)
     P, k = g.shape
+    mdt, mtype = MOMENTS[moments]
     idx = _c(idx, np.int64)
     assert idx.size == k
-    for a in (w, m, v):
-        assert a.dtype == np.float32 and a.flags.c_contiguous and a.size == k
+    assert w.dtype == np.float32 and w.flags.c_contiguous and w.size == k
+    for a in (m, v):
+        assert a.dtype == mtype and a.flags.c_contiguous and a.size == k
     gout = np.empty(k, np.float32)
     rep = np.empty(k, np.uint16)
     flag = np.zeros(1, np.int32)
-    rc = _load().ora_step_sampled(_ptr(g), _ptr(idx), k, gdt, _ptr(w), _ptr(m), _ptr(v),
-                                  _ptr(gout), _ptr(rep), n, P, scale, lr, b1, b2, eps, wd, t,
-                                  int(bool(skip)), _ptr(flag))
+    rc = _load().ora_step_sampled_mdt(_ptr(g), _ptr(idx), k, gdt, _ptr(w), _ptr(m), _ptr(v), mdt,
+                                      _ptr(gout), _ptr(rep), n, P, scale, lr, b1, b2, eps, wd, t,
+                                      int(bool(skip)), _ptr(flag))
     if rc != 0:
         raise ValueError("oracle step_sampled: bad arguments")
     return gout, rep, int(flag[0])

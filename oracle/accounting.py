@@ -25,8 +25,19 @@ STATE_BYTES = {
 }
 
 
-def bytes_per_param() -> int:
-    return sum(STATE_BYTES.values())
+# CS336 Lecture 7 notes, 8.4: everything except the fp32 master weight in
+# BF16 -- 12 bytes per parameter.
+STATE_BYTES_BF16_MOMENTS = {
+    "param_bf16": 2,
+    "grad_bf16": 2,
+    "master_fp32": 4,
+    "m_bf16": 2,
+    "v_bf16": 2,
+}
+
+
+def bytes_per_param(moments: str = "f32") -> int:
+    return sum((STATE_BYTES if moments == "f32" else STATE_BYTES_BF16_MOMENTS).values())
 
 
 def optimizer_bytes_per_param() -> int:
@@ -65,11 +76,13 @@ def zero3_bytes_per_rank(n: int, p: int, elem_bytes: int) -> float:
     return 3.0 * (p - 1) / p * n * elem_bytes
 
 
-def fused_step_bytes_per_param(P: int, grad_bytes: int = 2, param_bytes: int = 2) -> int:
+def fused_step_bytes_per_param(P: int, grad_bytes: int = 2, param_bytes: int = 2,
+                               moment_bytes: int = 4) -> int:
     """HBM bytes one fused step moves per parameter when the P ranks share one HBM.
 
-    Each rank's gradient is read once (P * grad_bytes), the fp32 master, m and
-    v are read and written once (12 + 12), and each rank's replica is written
-    once (P * param_bytes).
+    Each rank's gradient is read once (P * grad_bytes), the fp32 master and
+    the two moments are read and written once (2 * (4 + 2 * moment_bytes)),
+    and each rank's replica is written once (P * param_bytes).
     """
-    return P * grad_bytes + 12 + 12 + P * param_bytes
+    state = 4 + 2 * moment_bytes
+    return P * grad_bytes + state + state + P * param_bytes

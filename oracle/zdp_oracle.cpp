@@ -34,7 +34,11 @@
 //  * AdamW = the Adam of [F9] 9.2.2 plus decoupled weight decay applied to
 //    the pre-update weight: w <- w - (lr*wd)*w - lr*u;
 //  * bias corrections 1 - beta^t are evaluated in double and rounded to fp32;
-//  * fp32 -> bf16 is round-to-nearest-even; NaN becomes a quiet NaN.
+//  * fp32 -> bf16 is round-to-nearest-even; NaN becomes a quiet NaN;
+//  * with bf16 moments (CS336 Lecture 7 notes, 8.4: everything but the fp32
+//    master weight in BF16, 12 bytes per parameter) m and v are stored in
+//    bf16: widened exactly when loaded, updated in fp32, the update uses the
+//    fresh fp32 moments, and they are rounded to nearest even when stored.
 
 #include <cmath>
 #include <cstdint>
@@ -163,6 +167,20 @@ void adamw_element(float& w, float& m, float& v, float g, const Adam& a) {
   v = v_new;
 }
 
+// Moments stored as fp32 (mdt == 0) or bf16 bit patterns (mdt == 1).
+float load_moment(const void* base, int64_t k, int mdt) {
+  return mdt == 0 ? static_cast<const float*>(base)[k]
+                  : bf16_to_float(static_cast<const uint16_t*>(base)[k]);
+}
+
+void store_moment(void* base, int64_t k, int mdt, float x) {
+  if (mdt == 0) {
+    static_cast<float*>(base)[k] = x;
+  } else {
+    static_cast<uint16_t*>(base)[k] = float_to_bf16_rne(x);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -287,12 +305,13 @@ void ora_all_gather(const float* master, uint16_t* replicas, int64_t rld, int64_
 // element i is master[i - base]; replica row q (stride rld) likewise.  With
 // check_overflow != 0 and a non-finite reduced gradient anywhere in the
 // range, nothing is written.  Returns 0, or -1 on bad arguments.
-int ora_step(const uint16_t* grads, int64_t ld, int gdt, float* master, float* m, float* v,
-             uint16_t* replicas, int64_t rld, int64_t base, int64_t n, int64_t off, int64_t len,
-             int P,
-             float scale, float lr, float b1, float b2, float eps, float wd, int t,
-             int check_overflow, int32_t* overflow, double* sumsq) {
-  if (P < 1 || n < 1 || off < 0 || len < 0 || off + len > n || t < 1 || base > off) return -1;
+int ora_step_mdt(const uint16_t* grads, int64_t ld, int gdt, float* master, void* m, void* v,
+                 int mdt, uint16_t* replicas, int64_t rld, int64_t base, int64_t n, int64_t off,
+                 int64_t len, int P, float scale, float lr, float b1, float b2, float eps,
+                 float wd, int t, int check_overflow, int32_t* overflow, double* sumsq) {
+  if (P < 1 || n < 1 || off < 0 || len < 0 || off + len > n || t < 1 || base > off ||
+      (mdt != 0 && mdt != 1))
+    return -1;
   const int64_t S = shard_size(n, P);
   const Adam a = make_adam(lr, b1, b2, eps, wd, t);
   std::vector<float> vals(P);
@@ -311,11 +330,23 @@ int ora_step(const uint16_t* grads, int64_t ld, int gdt, float* master, float* m
   if (check_overflow && flag) return 0;
   for (int64_t j = 0; j < len; ++j) {
     const int64_t k = off + j - base;
-    adamw_element(master[k], m[k], v[k], g[j], a);
+    float mk = load_moment(m, k, mdt), vk = load_moment(v, k, mdt);
+    adamw_element(master[k], mk, vk, g[j], a);
+    store_moment(m, k, mdt, mk);
+    store_moment(v, k, mdt, vk);
     const uint16_t p = float_to_bf16_rne(master[k]);
     for (int q = 0; q < P; ++q) replicas[q * rld + k] = p;
   }
   return 0;
+}
+
+// The step with fp32 moments.
+int ora_step(const uint16_t* grads, int64_t ld, int gdt, float* master, float* m, float* v,
+             uint16_t* replicas, int64_t rld, int64_t base, int64_t n, int64_t off, int64_t len,
+             int P, float scale, float lr, float b1, float b2, float eps, float wd, int t,
+             int check_overflow, int32_t* overflow, double* sumsq) {
+  return ora_step_mdt(grads, ld, gdt, master, m, v, 0, replicas, rld, base, n, off, len, P, scale,
+                      lr, b1, b2, eps, wd, t, check_overflow, overflow, sumsq);
 }
 
 // The same step on a sample of k elements given by their global indices
@@ -323,11 +354,11 @@ int ora_step(const uint16_t* grads, int64_t ld, int gdt, float* master, float* m
 // w/m/v are the state values there and are updated in place unless `skip`;
 // gout receives the reduced gradient and rep the bf16 value every replica
 // must hold.  `skip` is the caller's skip decision for the whole step.
-int ora_step_sampled(const uint16_t* gs, const int64_t* idx, int64_t k, int gdt, float* w,
-                     float* m, float* v, float* gout, uint16_t* rep, int64_t n, int P, float scale,
-                     float lr, float b1, float b2, float eps, float wd, int t, int skip,
-                     int32_t* overflow) {
-  if (P < 1 || n < 1 || t < 1) return -1;
+int ora_step_sampled_mdt(const uint16_t* gs, const int64_t* idx, int64_t k, int gdt, float* w,
+                         void* m, void* v, int mdt, float* gout, uint16_t* rep, int64_t n, int P,
+                         float scale, float lr, float b1, float b2, float eps, float wd, int t,
+                         int skip, int32_t* overflow) {
+  if (P < 1 || n < 1 || t < 1 || (mdt != 0 && mdt != 1)) return -1;
   const int64_t S = shard_size(n, P);
   const Adam a = make_adam(lr, b1, b2, eps, wd, t);
   std::vector<float> vals(P);
@@ -338,11 +369,24 @@ int ora_step_sampled(const uint16_t* gs, const int64_t* idx, int64_t k, int gdt,
     const float g = ring_sum(vals.data(), P, owner_of(idx[j], S)) * scale;
     if (!is_finite(g)) flag = 1;
     gout[j] = g;
-    if (!skip) adamw_element(w[j], m[j], v[j], g, a);
+    if (!skip) {
+      float mj = load_moment(m, j, mdt), vj = load_moment(v, j, mdt);
+      adamw_element(w[j], mj, vj, g, a);
+      store_moment(m, j, mdt, mj);
+      store_moment(v, j, mdt, vj);
+    }
     rep[j] = float_to_bf16_rne(w[j]);
   }
   if (overflow) *overflow |= flag;
   return 0;
+}
+
+int ora_step_sampled(const uint16_t* gs, const int64_t* idx, int64_t k, int gdt, float* w,
+                     float* m, float* v, float* gout, uint16_t* rep, int64_t n, int P, float scale,
+                     float lr, float b1, float b2, float eps, float wd, int t, int skip,
+                     int32_t* overflow) {
+  return ora_step_sampled_mdt(gs, idx, k, gdt, w, m, v, 0, gout, rep, n, P, scale, lr, b1, b2,
+                              eps, wd, t, skip, overflow);
 }
 
 }  // extern "C"

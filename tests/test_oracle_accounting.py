@@ -27,3 +27,9 @@ def test_fused_step_bytes():
     # 2P gradient reads + 12 state reads + 12 state writes + 2P replica writes
     assert [accounting.fused_step_bytes_per_param(P) for P in (2, 4, 8, 16, 64)] == \
         [32, 40, 56, 88, 280]
+
+
+def test_twelve_bytes_with_bf16_moments():
+    # CS336 Lecture 7 notes, 8.4: all but the master weight in BF16
+    assert accounting.bytes_per_param("bf16") == 12
+    assert accounting.fused_step_bytes_per_param(8, moment_bytes=2) == 48
