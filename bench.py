@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gpt_1p3b")
+    ap.add_argument("--moments", choices=("f32", "bf16"), default="f32",
+                    help="storage of the AdamW moments (bf16: 12 bytes of state per parameter)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--e2e-bucket", type=int, default=1 << 26,
@@ -97,9 +99,10 @@ def whole_job_rate(units_per_rank: int, steps: int, world: int, slowest_ms: floa
     return world * units_per_rank * steps / (slowest_ms / 1e3)
 
 
-def bytes_per_param(P: int) -> int:
-    # P bf16 gradient reads + fp32 master/m/v read and written + P bf16 replica writes
-    return 2 * P + 12 + 12 + 2 * P
+def bytes_per_param(P: int, moments: str = "f32") -> int:
+    # P bf16 gradient reads + master/m/v read and written + P bf16 replica writes
+    state = 12 if moments == "f32" else 8
+    return 2 * P + state + state + 2 * P
 
 
 def config_of(wl, bucket_elems=0, l2_flush=False):
@@ -266,6 +269,11 @@ def run_ours(args):
     state = torch.empty(3, n_pad, dtype=torch.float32, device=dev)
     master, m, v = state[0], state[1], state[2]
     workloads.fill_state(master, m, v, wl, seed)
+    if args.moments == "bf16":  # the same moments, held in bf16
+        mv16 = state[1:].to(torch.bfloat16)
+        m, v = mv16[0], mv16[1]
+        state = state[:1].clone()
+        master = state[0]
     replicas = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
     words = torch.zeros(16, dtype=torch.uint8, device=dev)
     flag = words[0:4].view(torch.int32)
@@ -274,7 +282,7 @@ def run_ours(args):
 
     a, keep = zdp.make_step_args(grads, master, m, v, replicas, n=n, scale=wl.scale, t=1,
                                  bucket_elems=wl.bucket_elems, d_overflow=flag, d_sumsq=sumsq,
-                                 **HP)
+                                 moments=args.moments, **HP)
     # one fused launch per bucket (the whole range when the workload has no buckets)
     launches_per_step = -(-n // wl.bucket_elems) if wl.bucket_elems else 1
     stream = torch.cuda.current_stream(dev)
@@ -283,7 +291,7 @@ def run_ours(args):
     # launches alone with events.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = (torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-             if bytes_per_param(P) * n < 4 * l2 else None)
+             if bytes_per_param(P, args.moments) * n < 4 * l2 else None)
     t = 0
 
     def one_step(e0=None, e1=None):
@@ -337,6 +345,7 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t)
+        e2e["moments"] = args.moments
         slowest = max_over_ranks([e2e.get("seconds_per_step") or 0.0], dev)[0]
         if e2e.get("value") is not None:
             e2e["value"] = whole_job_rate(n, 1, world, slowest * 1e3)
@@ -345,9 +354,9 @@ def run_ours(args):
     out = None
     if rank == 0:
         peak, peak_kind = measured_peak()
-        alg_bytes = bytes_per_param(P) * n
+        alg_bytes = bytes_per_param(P, args.moments) * n
         achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
-        traffic = recorded_traffic(wl.name)
+        traffic = recorded_traffic(wl.name) if args.moments == "f32" else None
         clocks = sampler.summary(wall0, wall1)
         out = {
             "metric": METRIC,
@@ -363,7 +372,8 @@ def run_ours(args):
             "dtype": "f32",
             "data": "synthetic: seeded N(0, sigma_T) bf16 gradients (sigma_T log-uniform "
                     "[1e-5, 1e-2] per tensor), master ~ N(0, 0.02), m = v = 0 at t = 1",
-            "config": config_of(wl, wl.bucket_elems, flush is not None),
+            "config": dict(config_of(wl, wl.bucket_elems, flush is not None),
+                           moments=args.moments),
             "hbm_tbs": alg_bytes / (ms_per_step / 1e3) / 1e12,
             "roofline": {
                 "bound": "hbm",
@@ -384,7 +394,7 @@ def run_ours(args):
         if e2e is not None:
             out["e2e"] = e2e
         if world == 1 and not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(args, wl, grads, state, P, n)
+            out["cpu_baseline"] = cpu_baseline(args, wl, grads, master, m, v, P, n)
         if wl.name != workloads.gpt_1p3b().name:
             out["metric_note"] = f"measured on the {wl.name} workload, not the 1.3B headline"
     if world > 1:
@@ -486,7 +496,7 @@ def run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t0
 
     # zero-copy: one zdp_step whose gradient pointers are the pinned host buffers
     a0, keep0 = zdp.make_step_args(host, master, m, v, replicas, n=n, scale=wl.scale, t=1,
-                                   d_overflow=flag, d_sumsq=sumsq, **HP)
+                                   d_overflow=flag, d_sumsq=sumsq, moments=args.moments, **HP)
 
     def step_zero_copy():
         nonlocal t
@@ -503,7 +513,7 @@ def run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t0
     bounds = [(lo, min(n, lo + B)) for lo in range(0, n, B)]
     argv = [zdp.make_step_args([g[lo:hi] for g in grads], master, m, v, replicas, n=n,
                                scale=wl.scale, t=1, off=lo, length=hi - lo, d_overflow=flag,
-                               d_sumsq=sumsq, **HP) for lo, hi in bounds]
+                               d_sumsq=sumsq, moments=args.moments, **HP) for lo, hi in bounds]
     copy = torch.cuda.Stream(dev)
 
     def step_memcpy():
@@ -549,7 +559,7 @@ def _oracle_slice(P, S, n, length):
     return lo, min(length, n - lo)
 
 
-def cpu_baseline(args, wl, grads, state, P, n):
+def cpu_baseline(args, wl, grads, master, m, v, P, n):
     """The CPU oracle, as it is, on one host core, over a slice of the same
     workload straddling the boundary between rank 0's and rank 1's shards."""
     import numpy as np
@@ -559,15 +569,21 @@ def cpu_baseline(args, wl, grads, state, P, n):
 
     S = -(-n // P)
     lo, length = _oracle_slice(P, S, n, args.cpu_sample)
-    g = np.stack([grads[q][lo:lo + length].view(torch.int16).cpu().numpy().view(np.uint16)
-                  for q in range(P)])
-    w, m, v = (state[k, lo:lo + length].cpu().numpy().copy() for k in range(3))
+
+    def host(t):
+        x = t[lo:lo + length]
+        if x.dtype == torch.float32:
+            return x.cpu().numpy().copy()
+        return x.view(torch.int16).cpu().numpy().view(np.uint16).copy()
+
+    g = np.stack([host(grads[q]) for q in range(P)])
+    w, mh, vh = host(master), host(m), host(v)
     rep = np.empty((P, length), np.uint16)
     oracle.build()
     steps, t0 = 0, time.perf_counter()
     while True:
-        oracle.step(g, oracle.BF16, w, m, v, rep, n, lo, length, wl.scale, t=steps + 1,
-                    base=lo, **HP)
+        oracle.step(g, oracle.BF16, w, mh, vh, rep, n, lo, length, wl.scale, t=steps + 1,
+                    base=lo, moments=args.moments, **HP)
         steps += 1
         el = time.perf_counter() - t0
         if el >= args.cpu_seconds:

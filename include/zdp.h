@@ -66,6 +66,16 @@ typedef enum zdp_dtype {
   ZDP_FP16 = 1  /* IEEE binary16 gradients (loss-scaled training) */
 } zdp_dtype;
 
+/* Storage of the AdamW moments m and v.  ZDP_MOMENTS_BF16 keeps everything
+ * except the fp32 master weight in bf16, 12 bytes of state per parameter
+ * (CS336 Lecture 7 notes, 8.4): the moments are widened exactly on load,
+ * updated in fp32 (the update uses these fp32 values), and rounded to
+ * nearest even when stored. */
+typedef enum zdp_moment_dtype {
+  ZDP_MOMENTS_F32 = 0,
+  ZDP_MOMENTS_BF16 = 1
+} zdp_moment_dtype;
+
 enum {
   ZDP_OK = 0,
   ZDP_ERR_INVALID = -1,
@@ -125,8 +135,8 @@ typedef struct zdp_step_args {
                                  q's gradient of global element off+j, j < len */
   int gdt;                    /* zdp_dtype of the gradients */
   float* master;              /* device fp32, >= n elements, indexed by global element */
-  float* m;                   /* device fp32, >= n elements */
-  float* v;                   /* device fp32, >= n elements */
+  void* m;                    /* device, >= n elements: fp32, or bf16 per moment_dtype */
+  void* v;                    /* device, >= n elements: fp32, or bf16 per moment_dtype */
   uint16_t* const* replicas;  /* host array of P device pointers, >= n bf16 each,
                                  indexed by global element */
   int64_t n;                  /* model size; fixes S = ceil(n/P) and so the owners */
@@ -147,6 +157,7 @@ typedef struct zdp_step_args {
   void* workspace;            /* device scratch for check_overflow (else unused), at
                                  least zdp_step_workspace_bytes() bytes, 16-B aligned */
   size_t workspace_bytes;
+  int moment_dtype;           /* zdp_moment_dtype of m and v (0: fp32) */
 } zdp_step_args;
 
 /* Scratch bytes zdp_step needs for these arguments: 0 without
@@ -180,8 +191,9 @@ int zdp_step(const zdp_step_args* args, void* stream);
  * The partial sums travel through `workspace` (2*P*S fp32 "messages",
  * zdp_step_ring_workspace_bytes(args) bytes, 16-byte aligned).
  * Results are bit-identical to zdp_step (same additions in the same order).
- * The call covers the whole model: off = 0, len = n, bucket_elems = 0 and
- * check_overflow = 0 are required (ZDP_ERR_INVALID otherwise); d_overflow and
+ * The call covers the whole model: off = 0, len = n, bucket_elems = 0,
+ * check_overflow = 0 and fp32 moments are required (ZDP_ERR_INVALID
+ * otherwise); d_overflow and
  * d_sumsq work as for zdp_step.  With bf16 gradients it moves about
  * (14P + 14) bytes of HBM traffic per parameter (each of the P-2 middle
  * reduce-scatter steps reads and writes the fp32 messages), against

@@ -91,11 +91,13 @@ class DeviceStep:
     """Device buffers of one step problem: P gradients (bf16/fp16), fp32
     master/m/v of n_pad elements, P bf16 replicas, flag and sum of squares."""
 
-    def __init__(self, P: int, n: int, gdtype=torch.bfloat16, device="cuda", misalign=False):
+    def __init__(self, P: int, n: int, gdtype=torch.bfloat16, device="cuda", misalign=False,
+                 moments="f32"):
         self.P, self.n = P, n
         self.S = -(-n // P)
         self.n_pad = P * self.S
         self.device = device
+        self.moments = moments
         extra = 1 if misalign else 0
         self._g = [torch.zeros(n + extra, dtype=gdtype, device=device) for _ in range(P)]
         self._r = [torch.zeros(n + extra, dtype=torch.bfloat16, device=device) for _ in range(P)]
@@ -103,8 +105,13 @@ class DeviceStep:
         self.grads = [g[extra:] for g in self._g]
         self.replicas = [r[extra:] for r in self._r]
         self.master = self._st[0, extra:extra + self.n_pad]
-        self.m = self._st[1, extra:extra + self.n_pad]
-        self.v = self._st[2, extra:extra + self.n_pad]
+        if moments == "f32":
+            self.m = self._st[1, extra:extra + self.n_pad]
+            self.v = self._st[2, extra:extra + self.n_pad]
+        else:  # bf16 moments, separate buffers
+            self._mv = torch.zeros(2, self.n_pad + 8 * extra, dtype=torch.bfloat16, device=device)
+            self.m = self._mv[0, extra:extra + self.n_pad]
+            self.v = self._mv[1, extra:extra + self.n_pad]
         self.flag = torch.zeros(1, dtype=torch.int32, device=device)
         self.sumsq = torch.zeros(1, dtype=torch.float64, device=device)
 
@@ -112,14 +119,20 @@ class DeviceStep:
         for q in range(self.P):
             self.grads[q].copy_(tensor_from_bits(gbits[q, :self.n], self.grads[q].dtype, "cpu"))
         self.master.copy_(torch.from_numpy(np.asarray(w, np.float32)))
-        self.m.copy_(torch.from_numpy(np.asarray(m, np.float32)))
-        self.v.copy_(torch.from_numpy(np.asarray(v, np.float32)))
+        if self.moments == "f32":
+            self.m.copy_(torch.from_numpy(np.asarray(m, np.float32)))
+            self.v.copy_(torch.from_numpy(np.asarray(v, np.float32)))
+        else:  # m, v given as bf16 bit patterns
+            self.m.copy_(tensor_from_bits(np.asarray(m, np.uint16), torch.bfloat16, "cpu"))
+            self.v.copy_(tensor_from_bits(np.asarray(v, np.uint16), torch.bfloat16, "cpu"))
         if rep_bits is not None:
             for q in range(self.P):
                 self.replicas[q].copy_(tensor_from_bits(rep_bits[q], torch.bfloat16, "cpu"))
 
     def state(self):
-        return (self.master.cpu().numpy(), self.m.cpu().numpy(), self.v.cpu().numpy())
+        if self.moments == "f32":
+            return (self.master.cpu().numpy(), self.m.cpu().numpy(), self.v.cpu().numpy())
+        return (self.master.cpu().numpy(), bits_of(self.m), bits_of(self.v))
 
     def replica_bits(self) -> np.ndarray:
         return np.stack([bits_of(r) for r in self.replicas])
@@ -133,7 +146,7 @@ class DeviceStep:
             grads, self.master, self.m, self.v, self.replicas, n=self.n, scale=scale, t=t,
             off=off, length=length, bucket_elems=bucket_elems, check_overflow=check_overflow,
             d_overflow=self.flag if with_flag else None,
-            d_sumsq=self.sumsq if with_sumsq else None, **hp)
+            d_sumsq=self.sumsq if with_sumsq else None, moments=self.moments, **hp)
         if check_overflow:
             nbytes = zdp.zdp_step_workspace_bytes(a)
             if workspace is None:

@@ -63,26 +63,43 @@ def gather_f32(t, idx_dev):
 class Problem:
     """Full-size device buffers of one workload."""
 
-    def __init__(self, wl, seed, grads=True):
+    def __init__(self, wl, seed, grads=True, moments="f32"):
         self.wl, self.P, self.n = wl, wl.P, wl.n
         self.S = -(-wl.n // wl.P)
+        self.moments = moments
         gdt = torch.float16 if wl.grad_dtype == "fp16" else torch.bfloat16
         self.grads = ([torch.empty(wl.n, dtype=gdt, device=DEV) for _ in range(wl.P)]
                       if grads else None)
         self.state = torch.empty(3, self.P * self.S, dtype=torch.float32, device=DEV)
         workloads.fill_state(self.state[0], self.state[1], self.state[2], wl, seed)
+        if moments == "bf16":  # the same moments, held in bf16
+            self.mv16 = self.state[1:].to(torch.bfloat16)
+            self.state = self.state[:1].clone()
         self.replicas = [torch.full((wl.n,), 0.5, dtype=torch.bfloat16, device=DEV)
                          for _ in range(wl.P)]
         self.words = torch.zeros(16, dtype=torch.uint8, device=DEV)
         self.flag = self.words[0:4].view(torch.int32)
         self.sumsq = self.words[8:16].view(torch.float64)
 
+    def buffers(self):
+        if self.moments == "f32":
+            return self.state[0], self.state[1], self.state[2]
+        return self.state[0], self.mv16[0], self.mv16[1]
+
     def oracle_state(self, idx_dev):
-        return [gather_f32(self.state[k], idx_dev).copy() for k in range(3)]
+        if self.moments == "f32":
+            return [gather_f32(self.state[k], idx_dev).copy() for k in range(3)]
+        return [gather_f32(self.state[0], idx_dev).copy(), gather_bits(self.mv16[0], idx_dev),
+                gather_bits(self.mv16[1], idx_dev)]
 
     def check(self, idx, idx_dev, ora_w, ora_m, ora_v, ora_rep, label):
-        for k, (name, want) in enumerate((("master", ora_w), ("m", ora_m), ("v", ora_v))):
-            assert_state_close(gather_f32(self.state[k], idx_dev), want, f"{label} {name}")
+        assert_state_close(gather_f32(self.state[0], idx_dev), ora_w, f"{label} master")
+        if self.moments == "f32":
+            for k, (name, want) in enumerate((("m", ora_m), ("v", ora_v)), start=1):
+                assert_state_close(gather_f32(self.state[k], idx_dev), want, f"{label} {name}")
+        else:
+            assert_bf16_close(gather_bits(self.mv16[0], idx_dev), ora_m, f"{label} m")
+            assert_bf16_close(gather_bits(self.mv16[1], idx_dev), ora_v, f"{label} v")
         reps = np.stack([gather_bits(r, idx_dev) for r in self.replicas])
         for q in range(self.P):
             assert_bf16_close(reps[q], ora_rep, f"{label} replica {q}")
@@ -117,19 +134,21 @@ def test_gpt2_small_bucketed_ten_steps():
     _free()
 
 
-def test_gpt_1p3b_bench_configuration():
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+def test_gpt_1p3b_bench_configuration(moments):
     # one fused zdp_step over the whole model per step, flag and sum of
-    # squares on, no buckets: the call the benchmark times
+    # squares on, no buckets: the call the benchmark times (with fp32 or
+    # bf16 moments)
     wl = workloads.gpt_1p3b()
     seed = 3
-    pb = Problem(wl, seed)
+    pb = Problem(wl, seed, moments=moments)
     idx = sample_indices(pb.n, pb.S, pb.P, seed, extra=[t.offset for t in wl.tensors],
                          k_random=50_000, around=8)
     idx_dev = torch.from_numpy(idx).to(DEV)
     w, m, v = pb.oracle_state(idx_dev)
-    args, keep = zdp.make_step_args(pb.grads, pb.state[0], pb.state[1], pb.state[2],
-                                    pb.replicas, n=pb.n, scale=wl.scale, t=1,
-                                    d_overflow=pb.flag, d_sumsq=pb.sumsq, **HP)
+    args, keep = zdp.make_step_args(pb.grads, *pb.buffers(), pb.replicas, n=pb.n,
+                                    scale=wl.scale, t=1, d_overflow=pb.flag, d_sumsq=pb.sumsq,
+                                    moments=moments, **HP)
     for t in range(1, wl.steps + 1):
         for q in range(pb.P):
             workloads.fill_grads(pb.grads[q], wl, q, t, seed)
@@ -139,10 +158,10 @@ def test_gpt_1p3b_bench_configuration():
         zdp.zdp_step(args)
         torch.cuda.synchronize()
         gout, rep, flag = oracle.step_sampled(gs, idx, oracle.BF16, w, m, v, pb.n, wl.scale,
-                                              t=t, **HP)
+                                              t=t, moments=moments, **HP)
         assert flag == 0 and int(pb.flag.item()) == 0
         assert float(pb.sumsq.item()) > 0.0
-        pb.check(idx, idx_dev, w, m, v, rep, f"1.3B t={t}")
+        pb.check(idx, idx_dev, w, m, v, rep, f"1.3B {moments} moments t={t}")
     # the reduced gradients of the last step, bit for bit
     shards = torch.empty(pb.P * pb.S, dtype=torch.float32, device=DEV)
     zdp.zdp_reduce_scatter(pb.grads, shards, pb.n, pb.P, wl.scale)

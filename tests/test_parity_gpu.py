@@ -293,3 +293,30 @@ def test_sum_of_squares_over_extreme_magnitudes():
     dev.sumsq.zero_()
     dev.step(0.25, 3)
     assert abs(float(dev.sumsq.item()) - ss) <= 1e-9 * ss
+
+
+# ------------------------------------------------ 12 bytes/param: bf16 moments
+
+@pytest.mark.parametrize("P", [2, 5, 8, 64])
+def test_bf16_moments_fused_and_checked(P):
+    for n, gdt in ((P * 8 * 61 + 5, oracle.BF16), (40_003, oracle.FP16), (1 << 16, oracle.BF16)):
+        gbits, w, m32, v32 = random_problem(P, n, P * 1000 + n, gdt)
+        m16, v16 = oracle.f32_to_bf16(m32), oracle.f32_to_bf16(v32)
+        scale = 1.0 / (P * (65536.0 if gdt == oracle.FP16 else 1.0))
+        for check in (False, True):
+            dev = DeviceStep(P, n, torch.float16 if gdt == oracle.FP16 else torch.bfloat16,
+                             moments="bf16")
+            rep = np.zeros((P, n), np.uint16)
+            dev.load(gbits, w, m16, v16, rep)
+            dev.step(scale, 4, check_overflow=check)
+            ww, mm, vv, rr = w.copy(), m16.copy(), v16.copy(), rep.copy()
+            flag, ss = oracle.step(gbits, gdt, ww, mm, vv, rr, n, 0, n, scale, t=4,
+                                   check_overflow=check, moments="bf16", **HP)
+            label = f"bf16 moments P={P} n={n} check={check}"
+            gw, gm, gv = dev.state()
+            assert_state_close(gw, ww, label + " master")
+            assert_bf16_close(gm, mm, label + " m")
+            assert_bf16_close(gv, vv, label + " v")
+            assert_bf16_close(dev.replica_bits(), rr, label + " replicas")
+            assert int(dev.flag.item()) == flag
+            assert abs(float(dev.sumsq.item()) - ss) <= 1e-9 * ss

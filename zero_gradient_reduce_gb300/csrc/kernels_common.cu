@@ -60,7 +60,9 @@ cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cuda
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
   const void* fn = vec ? reinterpret_cast<const void*>(&k_adam_gather<true>)
                        : reinterpret_cast<const void*>(&k_adam_gather<false>);
-  return launch_fn(fn, p, vec, num_sms, p.nrep > 0 ? ZDP_CAP_ADAM_GATHER : ZDP_CAP_ADAM, s);
+  const int cap = p.nrep == 0 ? ZDP_CAP_ADAM
+                  : (p.mt == ZDP_MOMENTS_F32 ? ZDP_CAP_ADAM_GATHER : ZDP_CAP_ADAM_GATHER_BF16M);
+  return launch_fn(fn, p, vec, num_sms, cap, s);
 }
 
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {

@@ -197,6 +197,7 @@ int zdp_adamw_shard(float* master, float* m, float* v, const float* grad_shard, 
   p.w = master;
   p.m = m;
   p.v = v;
+  p.mt = ZDP_MOMENTS_F32;
   p.gin = grad_shard;
   p.gin_base = 0;
   p.lo = 0;
@@ -271,17 +272,18 @@ int validate_step(const zdp_step_args* a, size_t ws_need, bool* vec_out) {
   if (a->bucket_elems < 0) return fail(ZDP_ERR_INVALID, "bucket_elems < 0");
   if (!a->grads || !a->replicas) return fail(ZDP_ERR_INVALID, "grads or replicas is NULL");
   if (!a->master || !a->m || !a->v) return fail(ZDP_ERR_INVALID, "master, m or v is NULL");
+  if (a->moment_dtype != ZDP_MOMENTS_F32 && a->moment_dtype != ZDP_MOMENTS_BF16)
+    return fail(ZDP_ERR_INVALID, "bad moment type %d", a->moment_dtype);
   const int64_t n = a->n, off = a->off, len = a->len;
-  const float* st[3] = {a->master, a->m, a->v};
-  bool vec = true;
-  for (const float* b : st) {
-    if ((addr(b) & 3u) != 0) return fail(ZDP_ERR_INVALID, "fp32 state not 4-byte aligned");
-    vec = vec && aligned16(b);
-  }
+  const int64_t mbytes = a->moment_dtype == ZDP_MOMENTS_F32 ? 4 : 2;
+  if ((addr(a->master) & 3u) != 0) return fail(ZDP_ERR_INVALID, "master not 4-byte aligned");
+  if ((addr(a->m) & (mbytes - 1)) != 0 || (addr(a->v) & (mbytes - 1)) != 0)
+    return fail(ZDP_ERR_INVALID, "m or v not aligned to its element size");
+  bool vec = aligned16(a->master) && aligned16(a->m) && aligned16(a->v);
   std::vector<Range> outs;
   add_range(outs, a->master, n * 4, "master", 0);
-  add_range(outs, a->m, n * 4, "m", 0);
-  add_range(outs, a->v, n * 4, "v", 0);
+  add_range(outs, a->m, n * mbytes, "m", 0);
+  add_range(outs, a->v, n * mbytes, "v", 0);
   for (int q = 0; q < P; ++q) {
     if (!a->grads[q]) return fail(ZDP_ERR_INVALID, "grads[%d] is NULL", q);
     if (!a->replicas[q]) return fail(ZDP_ERR_INVALID, "replicas[%d] is NULL", q);
@@ -321,7 +323,8 @@ extern "C" {
 int zdp_step(const zdp_step_args* a, void* stream) {
   if (a && a->len == 0 && a->P >= 1 && a->P <= ZDP_MAX_P && a->n >= 1 && a->off >= 0 &&
       a->off <= a->n && a->t >= 1 && a->grads && a->replicas && a->master && a->m && a->v &&
-      (a->gdt == ZDP_BF16 || a->gdt == ZDP_FP16) && a->bucket_elems >= 0)
+      (a->gdt == ZDP_BF16 || a->gdt == ZDP_FP16) && a->bucket_elems >= 0 &&
+      (a->moment_dtype == ZDP_MOMENTS_F32 || a->moment_dtype == ZDP_MOMENTS_BF16))
     return ok();
   bool vec = false;
   if (validate_step(a, zdp_step_workspace_bytes(a), &vec) != ZDP_OK) return ZDP_ERR_INVALID;
@@ -342,6 +345,7 @@ int zdp_step(const zdp_step_args* a, void* stream) {
   p.w = a->master;
   p.m = a->m;
   p.v = a->v;
+  p.mt = a->moment_dtype;
   p.S = S;
   p.inv_s = 1.0f / static_cast<float>(S);
   p.P = P;
@@ -405,6 +409,8 @@ int zdp_step_ring(const zdp_step_args* a, void* stream) {
     return fail(ZDP_ERR_INVALID, "the ring schedule covers the whole model: off = 0, len = n");
   if (a->check_overflow) return fail(ZDP_ERR_INVALID, "zdp_step_ring has no overflow check");
   if (a->bucket_elems != 0) return fail(ZDP_ERR_INVALID, "zdp_step_ring takes no buckets");
+  if (a->moment_dtype != ZDP_MOMENTS_F32)
+    return fail(ZDP_ERR_INVALID, "zdp_step_ring takes fp32 moments only");
   bool vec = false;
   if (validate_step(a, zdp_step_ring_workspace_bytes(a), &vec) != ZDP_OK) return ZDP_ERR_INVALID;
   int sms = 0;

@@ -28,6 +28,21 @@ constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming ker
 #ifndef ZDP_CAP_FUSED_SMALL_P
 #define ZDP_CAP_FUSED_SMALL_P 5
 #endif
+#ifndef ZDP_CAP_FUSED_BF16M_SMALL_P
+#define ZDP_CAP_FUSED_BF16M_SMALL_P 12
+#endif
+#ifndef ZDP_CAP_ADAM_GATHER_BF16M
+#define ZDP_CAP_ADAM_GATHER_BF16M 7
+#endif
+
+// Blocks per SM of the fused step for P ranks and the moment type, from the
+// measurements above (bf16 moments leave fewer bytes in flight per thread
+// and want more threads: 8 blocks at P = 4..7, 7 at P = 8..15, 6 above).
+inline int fused_cap(int P, int mt) {
+  if (mt == ZDP_MOMENTS_F32) return P <= 3 ? ZDP_CAP_FUSED_SMALL_P : ZDP_CAP_FUSED;
+  if (P <= 3) return ZDP_CAP_FUSED_BF16M_SMALL_P;
+  return P < 8 ? 8 : (P < 16 ? 7 : 6);
+}
 #ifndef ZDP_CAP_REDUCE
 #define ZDP_CAP_REDUCE 12
 #endif
@@ -62,8 +77,9 @@ struct KParams {
   // rank q's replica of global element i: rep[q][i]
   uint16_t* rep[ZDP_MAX_P];
   float* w;  // master: w[i]
-  float* m;  // first moment: m[i]
-  float* v;  // second moment: v[i]
+  void* m;   // first moment m[i]: fp32, or bf16 when mt == ZDP_MOMENTS_BF16
+  void* v;   // second moment v[i], same type
+  int mt;    // zdp_moment_dtype of m and v
   const float* gin;  // reduced gradient input: gin[i - gin_base]
   float* gout;       // reduced gradient output: gout[i - gout_base]
   int64_t goff, gin_base, gout_base;

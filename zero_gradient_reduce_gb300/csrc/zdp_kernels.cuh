@@ -264,6 +264,45 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[kVec]) {
 }
 
 // ---------------------------------------------------------------------------
+// AdamW moments stored as fp32 or bf16 (p.mt is uniform over the grid).  bf16
+// moments are widened exactly and stored rounded to nearest even.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ld_moments8(const KParams& p, int64_t i0, float (&m)[kVec],
+                                            float (&v)[kVec]) {
+  if (p.mt == ZDP_MOMENTS_F32) {
+    ld_f8(static_cast<const float*>(p.m) + i0, m);
+    ld_f8(static_cast<const float*>(p.v) + i0, v);
+  } else {
+    vec_set<ZDP_BF16>(m, ld16(static_cast<const uint16_t*>(p.m) + i0));
+    vec_set<ZDP_BF16>(v, ld16(static_cast<const uint16_t*>(p.v) + i0));
+  }
+}
+
+__device__ __forceinline__ void st_moments8(const KParams& p, int64_t i0, const float (&m)[kVec],
+                                            const float (&v)[kVec]) {
+  if (p.mt == ZDP_MOMENTS_F32) {
+    st_f8(static_cast<float*>(p.m) + i0, m);
+    st_f8(static_cast<float*>(p.v) + i0, v);
+  } else {
+    st16(static_cast<uint16_t*>(p.m) + i0, pack_bf16x8(m));
+    st16(static_cast<uint16_t*>(p.v) + i0, pack_bf16x8(v));
+  }
+}
+
+__device__ __forceinline__ float ld_moment(const void* base, int64_t i, int mt) {
+  return mt == ZDP_MOMENTS_F32 ? static_cast<const float*>(base)[i]
+                               : widen1<ZDP_BF16>(static_cast<const uint16_t*>(base)[i]);
+}
+
+__device__ __forceinline__ void st_moment(void* base, int64_t i, int mt, float x) {
+  if (mt == ZDP_MOMENTS_F32) {
+    static_cast<float*>(base)[i] = x;
+  } else {
+    static_cast<uint16_t*>(base)[i] = to_bf16(x);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Flag and sum-of-squares accounting, one atomic per block at most.
 //
 // GB300 executes fp64 at a small fraction of its fp32 rate, so the sum of
@@ -373,11 +412,11 @@ __device__ __forceinline__ void fused_elem(const KParams& p, int P, int64_t i, b
   const int r = owner_of(i, p, P);
   const float g = __fmul_rn(ring_sum_elem<GT>(p, P, r, i), p.scale);
   account1(g, sq, bad, ss);
-  float w = p.w[i], m = p.m[i], v = p.v[i];
+  float w = p.w[i], m = ld_moment(p.m, i, p.mt), v = ld_moment(p.v, i, p.mt);
   adamw(w, m, v, g, p.ad);
   p.w[i] = w;
-  p.m[i] = m;
-  p.v[i] = v;
+  st_moment(p.m, i, p.mt, m);
+  st_moment(p.v, i, p.mt, v);
   const uint16_t b = to_bf16(w);
   for (int q = 0; q < P; ++q) p.rep[q][i] = b;
 }
@@ -399,8 +438,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
       if (i0 >= p.lo && i0 + kVec <= p.hi && i0 + kVec <= static_cast<int64_t>(r + 1) * p.S) {
         float w[kVec], m[kVec], v[kVec], g[kVec];
         ld_f8(p.w + i0, w);
-        ld_f8(p.m + i0, m);
-        ld_f8(p.v + i0, v);
+        ld_moments8(p, i0, m, v);
         ring_sum_vec<PT, EXACT, GT>(p, P, r, i0, g);
 #pragma unroll
         for (int k = 0; k < kVec; ++k) g[k] = __fmul_rn(g[k], p.scale);
@@ -408,8 +446,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
 #pragma unroll
         for (int k = 0; k < kVec; ++k) adamw(w[k], m[k], v[k], g[k], p.ad);
         st_f8(p.w + i0, w);
-        st_f8(p.m + i0, m);
-        st_f8(p.v + i0, v);
+        st_moments8(p, i0, m, v);
         const uint4 b = pack_bf16x8(w);
 #pragma unroll 8
         for (int q = 0; q < P; ++q) st16(p.rep[q] + i0, b);
@@ -485,14 +522,12 @@ __global__ void __launch_bounds__(kThreads) k_adam_gather(const __grid_constant_
       if (i0 >= p.lo && i0 + kVec <= p.hi) {
         float w[kVec], m[kVec], v[kVec], g[kVec];
         ld_f8(p.w + i0, w);
-        ld_f8(p.m + i0, m);
-        ld_f8(p.v + i0, v);
+        ld_moments8(p, i0, m, v);
         ld_f8(p.gin + (i0 - p.gin_base), g);
 #pragma unroll
         for (int k = 0; k < kVec; ++k) adamw(w[k], m[k], v[k], g[k], p.ad);
         st_f8(p.w + i0, w);
-        st_f8(p.m + i0, m);
-        st_f8(p.v + i0, v);
+        st_moments8(p, i0, m, v);
         if (p.nrep > 0) {
           const uint4 b = pack_bf16x8(w);
           for (int q = 0; q < p.nrep; ++q) st16(p.rep[q] + i0, b);
@@ -501,11 +536,11 @@ __global__ void __launch_bounds__(kThreads) k_adam_gather(const __grid_constant_
         for (int k = 0; k < kVec; ++k) {
           const int64_t i = i0 + k;
           if (i >= p.lo && i < p.hi) {
-            float w = p.w[i], m = p.m[i], v = p.v[i];
+            float w = p.w[i], m = ld_moment(p.m, i, p.mt), v = ld_moment(p.v, i, p.mt);
             adamw(w, m, v, p.gin[i - p.gin_base], p.ad);
             p.w[i] = w;
-            p.m[i] = m;
-            p.v[i] = v;
+            st_moment(p.m, i, p.mt, m);
+            st_moment(p.v, i, p.mt, v);
             const uint16_t b = to_bf16(w);
             for (int q = 0; q < p.nrep; ++q) p.rep[q][i] = b;
           }
@@ -514,11 +549,11 @@ __global__ void __launch_bounds__(kThreads) k_adam_gather(const __grid_constant_
     }
   } else {
     for (int64_t i = p.lo + tid; i < p.hi; i += stride) {
-      float w = p.w[i], m = p.m[i], v = p.v[i];
+      float w = p.w[i], m = ld_moment(p.m, i, p.mt), v = ld_moment(p.v, i, p.mt);
       adamw(w, m, v, p.gin[i - p.gin_base], p.ad);
       p.w[i] = w;
-      p.m[i] = m;
-      p.v[i] = v;
+      st_moment(p.m, i, p.mt, m);
+      st_moment(p.v, i, p.mt, v);
       const uint16_t b = to_bf16(w);
       for (int q = 0; q < p.nrep; ++q) p.rep[q][i] = b;
     }

@@ -229,8 +229,8 @@ cudaError_t launch_ring(const zdp_step_args* a, const AdamK& ad, float* ws, bool
     p.rep[q] = a->replicas[q];
   }
   p.w = a->master;
-  p.m = a->m;
-  p.v = a->v;
+  p.m = static_cast<float*>(a->m);  // the ring mode takes fp32 moments only
+  p.v = static_cast<float*>(a->v);
   p.n = a->n;
   p.S = (a->n + P - 1) / P;
   p.P = P;

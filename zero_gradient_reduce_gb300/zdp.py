@@ -21,6 +21,8 @@ ZDP_ERR_CUDA = -2
 ZDP_MAX_P = 64
 ZDP_BF16 = 0
 ZDP_FP16 = 1
+ZDP_MOMENTS_F32 = 0
+ZDP_MOMENTS_BF16 = 1
 ZDP_NOALLOC_MAX_LEN = 16_777_216
 
 EXPORTS = (
@@ -61,6 +63,7 @@ class zdp_step_args(ctypes.Structure):
         ("d_sumsq", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("moment_dtype", ctypes.c_int),
     ]
 
 
@@ -188,8 +191,10 @@ def make_step_args(grads: Sequence[Ptr], master: Ptr, m: Ptr, v: Ptr, replicas: 
                    t: int, off: int = 0, length: Optional[int] = None, bucket_elems: int = 0,
                    check_overflow: bool = False, d_overflow: Ptr = None, d_sumsq: Ptr = None,
                    workspace: Ptr = None, workspace_bytes: int = 0,
-                   gdt: Optional[int] = None):
+                   gdt: Optional[int] = None, moments: str = "f32"):
     """Builds a zdp_step_args for the range [off, off+length) (default: to n).
+
+    moments: "f32" (m and v fp32) or "bf16" (m and v bf16 buffers).
 
     Returns (args, keepalive): the pointer arrays in `keepalive` back the
     struct's grads/replicas fields and must outlive every use of `args`.
@@ -218,6 +223,7 @@ def make_step_args(grads: Sequence[Ptr], master: Ptr, m: Ptr, v: Ptr, replicas: 
     a.d_sumsq = _addr(d_sumsq)
     a.workspace = _addr(workspace)
     a.workspace_bytes = workspace_bytes
+    a.moment_dtype = {"f32": ZDP_MOMENTS_F32, "bf16": ZDP_MOMENTS_BF16}[moments]
     return a, (garr, rarr)
 
 
