@@ -75,12 +75,16 @@ def lib_path() -> str:
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load libzdp.so (compiling it first if it is missing or stale)."""
+    """Load libzdp.so (compiling it first if it is missing or stale).
+
+    ZDP_LIBRARY_PATH, when set, names another build of the library to load
+    instead (it is not rebuilt).
+    """
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB
-    if build_if_missing and not _build.up_to_date():
+    path = os.environ.get("ZDP_LIBRARY_PATH") or _build.LIB
+    if path == _build.LIB and build_if_missing and not _build.up_to_date():
         _build.build()
     if not os.path.exists(path):
         raise ZdpError(ZDP_ERR_CUDA, f"libzdp not built ({path}); run the package build")
