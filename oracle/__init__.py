@@ -71,6 +71,11 @@ def _load():
             "ora_step_sampled": (ctypes.c_int, [vp, vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, i64,
                                                 ctypes.c_int, f32, f32, f32, f32, f32, f32,
                                                 ctypes.c_int, ctypes.c_int, vp]),
+            "ora_quantize_blocks": (None, [vp, i64, vp, vp]),
+            "ora_dequantize_blocks": (None, [vp, vp, i64, vp]),
+            "ora_step_zpp": (ctypes.c_int, [vp, i64, vp, i64, vp, vp, vp, ctypes.c_int, vp, i64,
+                                            vp, i64, i64, i64, i64, i64, ctypes.c_int, f32, f32,
+                                            f32, f32, f32, f32, ctypes.c_int, vp, vp]),
             "ora_step_mdt": (ctypes.c_int, [vp, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp,
                                             i64, i64, i64, i64, i64, ctypes.c_int, f32, f32, f32,
                                             f32, f32, f32, ctypes.c_int, ctypes.c_int, vp, vp]),
@@ -246,3 +251,52 @@ def step_sampled(gs, idx, gdt, w, m, v, n, scale, lr, b1, b2, eps, wd, t, skip=F
     if rc != 0:
         raise ValueError("oracle step_sampled: bad arguments")
     return gout, rep, int(flag[0])
+
+
+# ---- ZeRO++ block quantization (blocks of 256 elements) -------------------------
+
+QBLOCK = 256
+
+
+def quantize_blocks(x):
+    """fp32 values -> (int8 q, fp32 scale per block of 256)."""
+    a = _c(x, np.float32)
+    q = np.empty(a.size, np.int8)
+    sc = np.empty(-(-a.size // QBLOCK), np.float32)
+    _load().ora_quantize_blocks(_ptr(a), a.size, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def dequantize_blocks(q, scales):
+    qq = _c(q, np.int8)
+    sc = _c(scales, np.float32)
+    out = np.empty(qq.size, np.float32)
+    _load().ora_dequantize_blocks(_ptr(qq), _ptr(sc), qq.size, _ptr(out))
+    return out
+
+
+def step_zpp(gq, gs, master, m, v, rq, rs, n, off, len_, scale, lr, b1, b2, eps, wd, t,
+             base=0, moments="f32"):
+    """The ZeRO++ step: int8-block gradients in, int8-block replicas out.
+
+    gq: [P, >=len_] int8 rows (elements off..off+len_); gs: [P, blocks] fp32
+    scales of those rows (block (off+j)//256 - off//256).  master/m/v hold
+    global elements from `base`; rq: [P, >= off+len_-base] int8 and rs: [P,
+    blocks] fp32 replica scales, block i//256 - base//256.  In place.
+    Returns (overflow, sumsq).
+    """
+    gq = np.ascontiguousarray(gq, np.int8)
+    gs = np.ascontiguousarray(gs, np.float32)
+    P = gq.shape[0]
+    mdt, mtype = MOMENTS[moments]
+    assert master.dtype == np.float32 and m.dtype == mtype and v.dtype == mtype
+    assert rq.dtype == np.int8 and rq.flags.c_contiguous and rs.dtype == np.float32
+    flag = np.zeros(1, np.int32)
+    ss = np.zeros(1, np.float64)
+    rc = _load().ora_step_zpp(_ptr(gq), gq.shape[1], _ptr(gs), gs.shape[1], _ptr(master),
+                              _ptr(m), _ptr(v), mdt, _ptr(rq), rq.shape[1], _ptr(rs),
+                              rs.shape[1], base, n, off, len_, P, scale, lr, b1, b2, eps, wd, t,
+                              _ptr(flag), _ptr(ss))
+    if rc != 0:
+        raise ValueError("oracle step_zpp: bad arguments")
+    return int(flag[0]), float(ss[0])

@@ -35,11 +35,20 @@
 //    the pre-update weight: w <- w - (lr*wd)*w - lr*u;
 //  * bias corrections 1 - beta^t are evaluated in double and rounded to fp32;
 //  * fp32 -> bf16 is round-to-nearest-even; NaN becomes a quiet NaN;
+//  * ZeRO++ ([F9] 9.4.3: weights quantized to INT8 before the all-gather and
+//    dequantized after it; gradients quantized block-wise for the
+//    reduce-scatter): blocks of 256 consecutive elements (global index i in
+//    block i / 256); scale = max|x| / 127 over the block (fp32 division),
+//    q = x / scale rounded half to even and clamped to [-127, 127]; an
+//    all-zero block has scale 0 and q = 0; dequantization is q * scale in
+//    fp32.  The quantized all-gather quantizes the bf16 parameter; a
+//    quantized gradient is dequantized in fp32 before the ring sum;
 //  * with bf16 moments (CS336 Lecture 7 notes, 8.4: everything but the fp32
 //    master weight in BF16, 12 bytes per parameter) m and v are stored in
 //    bf16: widened exactly when loaded, updated in fp32, the update uses the
 //    fresh fp32 moments, and they are rounded to nearest even when stored.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -166,6 +175,30 @@ void adamw_element(float& w, float& m, float& v, float g, const Adam& a) {
   m = m_new;
   v = v_new;
 }
+
+// ---------------------------------------------------------------------------
+// Block-wise int8 quantization (ZeRO++, [F9] 9.4.3).
+// ---------------------------------------------------------------------------
+constexpr int64_t kQBlock = 256;
+
+float quant_scale(const float* x, int64_t count) {
+  float amax = 0.0f;
+  for (int64_t k = 0; k < count; ++k) {
+    const float a = std::fabs(x[k]);
+    if (a > amax) amax = a;
+  }
+  return amax / 127.0f;
+}
+
+int8_t quant_one(float x, float scale) {
+  if (scale == 0.0f) return 0;
+  float r = std::nearbyint(x / scale);  // the default rounding mode: half to even
+  if (r > 127.0f) r = 127.0f;
+  if (r < -127.0f) r = -127.0f;
+  return static_cast<int8_t>(r);
+}
+
+float dequant_one(int8_t q, float scale) { return static_cast<float>(q) * scale; }
 
 // Moments stored as fp32 (mdt == 0) or bf16 bit patterns (mdt == 1).
 float load_moment(const void* base, int64_t k, int mdt) {
@@ -387,6 +420,71 @@ int ora_step_sampled(const uint16_t* gs, const int64_t* idx, int64_t k, int gdt,
                      int32_t* overflow) {
   return ora_step_sampled_mdt(gs, idx, k, gdt, w, m, v, 0, gout, rep, n, P, scale, lr, b1, b2,
                               eps, wd, t, skip, overflow);
+}
+
+// ---- ZeRO++ block quantization -----------------------------------------------
+// x[0..n) -> q[0..n), scales[0..ceil(n/256)): block b covers [256b, 256b+256).
+void ora_quantize_blocks(const float* x, int64_t n, int8_t* q, float* scales) {
+  for (int64_t b = 0; b * kQBlock < n; ++b) {
+    const int64_t lo = b * kQBlock, cnt = std::min<int64_t>(kQBlock, n - lo);
+    scales[b] = quant_scale(x + lo, cnt);
+    for (int64_t k = 0; k < cnt; ++k) q[lo + k] = quant_one(x[lo + k], scales[b]);
+  }
+}
+
+void ora_dequantize_blocks(const int8_t* q, const float* scales, int64_t n, float* x) {
+  for (int64_t i = 0; i < n; ++i) x[i] = dequant_one(q[i], scales[i / kQBlock]);
+}
+
+// The ZeRO++ step over the global range [off, off+len) of an n-element model
+// (off a multiple of 256; off+len a multiple of 256 or n).  Rank q's gradient
+// of element off+j is the int8 gq[q*ld + j] times the fp32 scale
+// gs[q*sld + (off+j)/256 - off/256]; master/m/v hold global elements from
+// `base` on (m/v fp32 or bf16 per mdt); rank q's replica of element i is the
+// int8 rq[q*rld + i - base] with scale rs[q*rsld + i/256 - base/256] (base a
+// multiple of 256), quantized from the bf16 parameter.  No overflow skip.
+int ora_step_zpp(const int8_t* gq, int64_t ld, const float* gs, int64_t sld, float* master,
+                 void* m, void* v, int mdt, int8_t* rq, int64_t rld, float* rs, int64_t rsld,
+                 int64_t base, int64_t n, int64_t off, int64_t len, int P, float scale, float lr,
+                 float b1, float b2, float eps, float wd, int t, int32_t* overflow,
+                 double* sumsq) {
+  if (P < 1 || n < 1 || off < 0 || len < 0 || off + len > n || t < 1 || base > off ||
+      off % kQBlock != 0 || base % kQBlock != 0 || ((off + len) % kQBlock != 0 && off + len != n) ||
+      (mdt != 0 && mdt != 1))
+    return -1;
+  const int64_t S = shard_size(n, P);
+  const Adam a = make_adam(lr, b1, b2, eps, wd, t);
+  std::vector<float> vals(P);
+  std::vector<float> p(static_cast<size_t>(len));
+  int32_t flag = 0;
+  double ss = 0.0;
+  for (int64_t j = 0; j < len; ++j) {
+    const int64_t i = off + j;
+    for (int q = 0; q < P; ++q)
+      vals[q] = dequant_one(gq[q * ld + j], gs[q * sld + i / kQBlock - off / kQBlock]);
+    const float g = ring_sum(vals.data(), P, owner_of(i, S)) * scale;
+    if (!is_finite(g)) flag = 1;
+    ss += static_cast<double>(g) * static_cast<double>(g);
+    const int64_t k = i - base;
+    float mk = load_moment(m, k, mdt), vk = load_moment(v, k, mdt);
+    adamw_element(master[k], mk, vk, g, a);
+    store_moment(m, k, mdt, mk);
+    store_moment(v, k, mdt, vk);
+    p[j] = bf16_to_float(float_to_bf16_rne(master[k]));  // the bf16 parameter
+  }
+  if (overflow) *overflow |= flag;
+  if (sumsq) *sumsq += ss;
+  for (int64_t lo = 0; lo < len; lo += kQBlock) {
+    const int64_t cnt = std::min<int64_t>(kQBlock, len - lo);
+    const int64_t blk = (off + lo) / kQBlock - base / kQBlock;
+    const float sc = quant_scale(p.data() + lo, cnt);
+    for (int q = 0; q < P; ++q) {
+      rs[q * rsld + blk] = sc;
+      for (int64_t e = 0; e < cnt; ++e)
+        rq[q * rld + off + lo + e - base] = quant_one(p[lo + e], sc);
+    }
+  }
+  return 0;
 }
 
 }  // extern "C"
