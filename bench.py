@@ -69,6 +69,9 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=1 << 24,
                     help="parameters per oracle step in the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--zpp", action="store_true",
+                    help="the ZeRO++ step (int8 block-quantized gradients in, int8 replicas out) "
+                         "on the workload instead of zdp_step")
     ap.add_argument("--ring-study", action="store_true",
                     help="fused step against the literal ring schedule (zdp_step_ring) for "
                          "P = 2..64: one JSON line per P")
@@ -788,10 +791,82 @@ def run_ring_study(args):
         torch.cuda.empty_cache()
 
 
+def run_zpp(args):
+    """zdp_step_zpp on the workload: each rank's bf16 gradient is block-quantized
+    to int8 once (outside the timed region, as the producer would); every
+    step reads the P int8 gradients and scales, updates the fp32 state and
+    writes P int8 replicas and scales.  One JSON line, like the main arm."""
+    import torch
+
+    from zero_gradient_reduce_gb300 import workloads, zdp
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    zdp.load()
+    wl = workloads.by_name(args.workload)
+    P, n = wl.P, wl.n
+    S = -(-n // P)
+    nb = -(-n // zdp.ZDP_QBLOCK)
+    gq, gs = [], []
+    for q in range(P):
+        g = workloads.fill_grads(torch.empty(n, dtype=torch.bfloat16, device=dev), wl, q, 0,
+                                 args.seed)
+        qq = torch.empty(n, dtype=torch.int8, device=dev)
+        sc = torch.empty(nb, dtype=torch.float32, device=dev)
+        zdp.zdp_quantize_blocks(g, zdp.ZDP_BF16, n, qq, sc)
+        del g
+        gq.append(qq)
+        gs.append(sc)
+    st = torch.empty(3, P * S, dtype=torch.float32, device=dev)
+    workloads.fill_state(st[0], st[1], st[2], wl, args.seed)
+    m, v = st[1], st[2]
+    if args.moments == "bf16":
+        mv16 = st[1:].to(torch.bfloat16)
+        m, v = mv16[0], mv16[1]
+    rq = [torch.empty(n, dtype=torch.int8, device=dev) for _ in range(P)]
+    rs = [torch.empty(nb, dtype=torch.float32, device=dev) for _ in range(P)]
+    words = torch.zeros(16, dtype=torch.uint8, device=dev)
+    a, keep = zdp.make_zpp_args(gq, gs, st[0], m, v, rq, rs, n=n, scale=wl.scale, t=1,
+                                d_overflow=words[0:4].view(torch.int32),
+                                d_sumsq=words[8:16].view(torch.float64), moments=args.moments,
+                                **HP)
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.warmup + args.steps)]
+    for k, (e0, e1) in enumerate(ev):
+        a.t = k + 1
+        words.zero_()
+        e0.record(stream)
+        zdp.zdp_step_zpp(a, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev[args.warmup:]) / args.steps
+    state_b = 24 if args.moments == "f32" else 16
+    bpp = 2 * P + state_b + 8 * P / zdp.ZDP_QBLOCK
+    peak, peak_kind = measured_peak()
+    achieved = bpp * n / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": METRIC, "value": n / (ms / 1e3), "unit": "params/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded bf16 gradients block-quantized to int8",
+        "config": dict(config_of(wl), moments=args.moments, zpp="int8 blocks of 256, both ways"),
+        "hbm_tbs": achieved / 1e3,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_param": bpp},
+        "gpu_launches": args.steps,
+        "metric_note": "ZeRO++ variant of the step (quantized communication), not the headline",
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.zpp:
+        run_zpp(args)
     elif args.sweep:
         run_sweep(args)
     elif args.ring_study:

@@ -63,7 +63,8 @@ extern "C" {
 
 typedef enum zdp_dtype {
   ZDP_BF16 = 0, /* bfloat16 gradients */
-  ZDP_FP16 = 1  /* IEEE binary16 gradients (loss-scaled training) */
+  ZDP_FP16 = 1, /* IEEE binary16 gradients (loss-scaled training) */
+  ZDP_F32 = 2   /* fp32 (input of zdp_quantize_blocks only) */
 } zdp_dtype;
 
 /* Storage of the AdamW moments m and v.  ZDP_MOMENTS_BF16 keeps everything
@@ -200,6 +201,61 @@ int zdp_step(const zdp_step_args* args, void* stream);
  * (4P + 24) for zdp_step. */
 size_t zdp_step_ring_workspace_bytes(const zdp_step_args* args);
 int zdp_step_ring(const zdp_step_args* args, void* stream);
+
+/* ZeRO++ (Fudan MLSys ch. 9, 9.4.3: the weights are converted to INT8
+ * before the all-gather and dequantized after it; gradients are quantized
+ * block-wise for the reduce-scatter).  Blocks are ZDP_QBLOCK = 256
+ * consecutive elements, global element i in block i / 256.  A block's scale
+ * is max|x| / 127 (fp32), q = x / scale rounded half to even and clamped to
+ * [-127, 127]; an all-zero block has scale 0; x is recovered as q * scale in
+ * fp32.  Non-finite values give unspecified q. */
+#define ZDP_QBLOCK 256
+
+/* Quantize n values (xdt: ZDP_BF16, ZDP_FP16 or ZDP_F32) into q (n int8)
+ * and scales (ceil(n/256) fp32, block b covering [256b, 256b+256)): the
+ * producer's side of the quantized reduce-scatter. */
+int zdp_quantize_blocks(const void* x, int xdt, int64_t n, int8_t* q, float* scales,
+                        void* stream);
+
+/* out[i] = bf16(q[i] * scales[i / 256]), rounded to nearest even: the
+ * receiver's side of the quantized all-gather. */
+int zdp_dequantize_blocks(const int8_t* q, const float* scales, int64_t n, uint16_t* out,
+                          void* stream);
+
+/* Arguments of the ZeRO++ step: as zdp_step_args, with int8 block-quantized
+ * gradients in and int8 block-quantized replicas out. */
+typedef struct zdp_zpp_args {
+  const int8_t* const* grads;      /* host array of P device pointers; grads[q][j] is rank
+                                      q's int8 gradient of global element off+j, j < len */
+  const float* const* grad_scales; /* host array of P device pointers; grad_scales[q][b] is
+                                      the scale of global block off/256 + b */
+  float* master;                   /* device fp32, >= n elements, global index */
+  void* m;                         /* device, >= n elements, fp32 or bf16 per moment_dtype */
+  void* v;
+  int moment_dtype;
+  int8_t* const* replicas;         /* host array of P device pointers, >= n int8 each;
+                                      global index */
+  float* const* replica_scales;    /* host array of P device pointers, >= ceil(n/256) fp32
+                                      each; global block index */
+  int64_t n, off, len;             /* off a multiple of 256; off+len a multiple of 256 or n */
+  int P;
+  float scale, lr, b1, b2, eps, wd;
+  int t;
+  int32_t* d_overflow;             /* nullable, as in zdp_step_args */
+  double* d_sumsq;                 /* nullable, as in zdp_step_args */
+} zdp_zpp_args;
+
+/* The step with quantized communication: element i's reduced gradient is
+ * the ring-order fp32 sum (as in zdp_step) of the P ranks' dequantized int8
+ * gradients, times scale; AdamW as in zdp_step; the new bf16 parameters are
+ * block-quantized once and the int8 values and scales written to every
+ * rank's replica.  HBM traffic per parameter: P int8 gradient reads, the
+ * state (24 bytes with fp32 moments, 16 with bf16), P int8 replica writes,
+ * and one fp32 scale per 256 elements per rank each way: 2P + 24 + P/32
+ * bytes with fp32 moments (40.25 at P = 8, against 56 for zdp_step).  All
+ * buffers must have element 0 on a 16-byte boundary (the scale arrays on a
+ * 4-byte one); no overflow skip (the flag is reported). */
+int zdp_step_zpp(const zdp_zpp_args* args, void* stream);
 
 /* Largest `len` zdp_step_noalloc accepts (16,777,216 elements). */
 #define ZDP_NOALLOC_MAX_LEN 16777216LL

@@ -139,3 +139,40 @@ def test_ring_rejects_bad_arguments(lib, mutate, needle):
 def test_ring_workspace_bytes(lib):
     a, keep = _args()  # n = 1000, P = 2: S = 500, two message sets of P*S fp32
     assert zdp.zdp_step_ring_workspace_bytes(a) == (2 * 2 * 500 * 4 + 255) // 256 * 256
+
+
+def _zpp_args(**kw):
+    P = 2
+    base = dict(n=1000, scale=0.5, t=1, lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
+    base.update(kw)
+    g = [FAKE + q * (1 << 20) for q in range(P)]
+    gs = [FAKE + (4 + q) * (1 << 20) for q in range(P)]
+    r = [FAKE + (8 + q) * (1 << 20) for q in range(P)]
+    rs = [FAKE + (12 + q) * (1 << 20) for q in range(P)]
+    return zdp.make_zpp_args(g, gs, FAKE + (100 << 20), FAKE + (104 << 20), FAKE + (108 << 20),
+                             r, rs, **base)
+
+
+@pytest.mark.parametrize("mutate,needle", [
+    (lambda a: (setattr(a, "off", 100), setattr(a, "len", 256)), "block"),
+    (lambda a: setattr(a, "len", 300), "block"),
+    (lambda a: setattr(a, "P", 0), "P=0"),
+    (lambda a: setattr(a, "t", 0), "t=0"),
+    (lambda a: setattr(a, "master", FAKE + (100 << 20) + 4), "16-byte"),
+    (lambda a: setattr(a, "m", FAKE + (8 << 20) + 512), "overlap"),
+    (lambda a: setattr(a, "moment_dtype", 5), "moment"),
+])
+def test_zpp_rejects_bad_arguments(lib, mutate, needle):
+    a, keep = _zpp_args()
+    mutate(a)
+    with pytest.raises(zdp.ZdpError, match=needle):
+        zdp.zdp_step_zpp(a, stream=0)
+
+
+def test_quantizer_rejects_bad_arguments(lib):
+    with pytest.raises(zdp.ZdpError, match="input type"):
+        zdp.zdp_quantize_blocks(FAKE, 7, 10, FAKE + 4096, FAKE + 8192, stream=0)
+    with pytest.raises(zdp.ZdpError, match="overlap"):
+        zdp.zdp_quantize_blocks(FAKE, zdp.ZDP_F32, 1000, FAKE + 16, FAKE + 8192, stream=0)
+    with pytest.raises(zdp.ZdpError, match="overlap"):
+        zdp.zdp_dequantize_blocks(FAKE, FAKE + 8192, 1000, FAKE + 500, stream=0)

@@ -1,0 +1,173 @@
+"""ZeRO++ on the GPU against the oracle (Fudan MLSys ch. 9, 9.4.3): block int8
+quantization and dequantization, and the step with quantized gradients in and
+quantized replicas out, element by element, including ragged ends, shard
+boundaries inside blocks, sub-ranges, bf16 moments and the 1.3B model."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import HP, assert_bits_equal, assert_state_close, bits_of
+from zero_gradient_reduce_gb300 import workloads, zdp
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda")
+
+
+def _i8(t):
+    return t.cpu().numpy().view(np.int8)
+
+
+@pytest.mark.parametrize("n", [1, 255, 256, 257, 256 * 77 + 13, 1 << 20])
+def test_quantize_and_dequantize_match_the_oracle(n):
+    rng = np.random.default_rng(n)
+    x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-6, 2, n)).astype(np.float32)
+    x[: min(n, 300)] *= 0  # a zero block (and part of the next)
+    for xdt, host in ((zdp.ZDP_F32, x), (zdp.ZDP_BF16, None)):
+        if xdt == zdp.ZDP_BF16:
+            xb = torch.from_numpy(x).to(torch.bfloat16)
+            dx = xb.to(DEV)
+            vals = xb.float().numpy()
+        else:
+            dx = torch.from_numpy(x).to(DEV)
+            vals = x
+        q = torch.empty(n, dtype=torch.int8, device=DEV)
+        sc = torch.empty(-(-n // 256), dtype=torch.float32, device=DEV)
+        zdp.zdp_quantize_blocks(dx, xdt, n, q, sc)
+        wq, ws = oracle.quantize_blocks(vals)
+        torch.cuda.synchronize()
+        assert np.array_equal(_i8(q), wq), f"q n={n} xdt={xdt}"
+        assert_bits_equal(sc.cpu().numpy(), ws, f"scales n={n}")
+        out = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+        zdp.zdp_dequantize_blocks(q, sc, n, out)
+        want = oracle.f32_to_bf16(oracle.dequantize_blocks(wq, ws))
+        assert np.array_equal(bits_of(out), want)
+
+
+def _zpp_problem(P, n, seed, moments="f32"):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((P, n)) * 1e-3 * 10.0 ** rng.uniform(-1, 1, (P, 1))).astype(np.float32)
+    qs = [oracle.quantize_blocks(x[r]) for r in range(P)]
+    gq = np.stack([a for a, _ in qs])
+    gs = np.stack([b for _, b in qs])
+    S = -(-n // P)
+    w = np.zeros(P * S, np.float32)
+    w[:n] = rng.standard_normal(n) * 0.02
+    m = np.zeros(P * S, np.float32)
+    v = np.zeros(P * S, np.float32)
+    m[:n] = rng.standard_normal(n) * 1e-4
+    v[:n] = rng.uniform(0, 1e-6, n)
+    if moments == "bf16":
+        m, v = oracle.f32_to_bf16(m), oracle.f32_to_bf16(v)
+    return gq, gs, w, m, v
+
+
+def _to_dev(gq, gs, w, m, v, P, n, moments):
+    dg = [torch.from_numpy(gq[q].view(np.uint8).copy()).to(DEV).view(torch.int8) for q in range(P)]
+    ds = [torch.from_numpy(gs[q].copy()).to(DEV) for q in range(P)]
+    dw = torch.from_numpy(w.copy()).to(DEV)
+    if moments == "f32":
+        dm, dv = torch.from_numpy(m.copy()).to(DEV), torch.from_numpy(v.copy()).to(DEV)
+    else:
+        dm = torch.from_numpy(m.view(np.int16).copy()).to(DEV).view(torch.bfloat16)
+        dv = torch.from_numpy(v.view(np.int16).copy()).to(DEV).view(torch.bfloat16)
+    nb = -(-n // 256)
+    rq = [torch.zeros(n, dtype=torch.int8, device=DEV) for _ in range(P)]
+    rs = [torch.zeros(nb, dtype=torch.float32, device=DEV) for _ in range(P)]
+    return dg, ds, dw, dm, dv, rq, rs
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 8, 12, 16])
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+def test_zpp_step_matches_the_oracle(P, moments):
+    for n in sorted({256 * P * 3 + 7, 40_000 + P, 256 * 64}):
+        gq, gs, w, m, v = _zpp_problem(P, n, P * n, moments)
+        dg, ds, dw, dm, dv, rq, rs = _to_dev(gq, gs, w, m, v, P, n, moments)
+        words = torch.zeros(16, dtype=torch.uint8, device=DEV)
+        a, keep = zdp.make_zpp_args(dg, ds, dw, dm, dv, rq, rs, n=n, scale=1.0 / P, t=4,
+                                    d_overflow=words[0:4].view(torch.int32),
+                                    d_sumsq=words[8:16].view(torch.float64), moments=moments, **HP)
+        zdp.zdp_step_zpp(a)
+        torch.cuda.synchronize()
+        nb = gs.shape[1]
+        wq, wsc = np.zeros((P, n), np.int8), np.zeros((P, nb), np.float32)
+        ww, mm, vv = w.copy(), m.copy(), v.copy()
+        flag, ss = oracle.step_zpp(gq, gs, ww, mm, vv, wq, wsc, n, 0, n, 1.0 / P, t=4,
+                                   moments=moments, **HP)
+        label = f"zpp P={P} n={n} {moments}"
+        assert_state_close(dw.cpu().numpy()[:n], ww[:n], label + " master")
+        if moments == "f32":
+            assert_state_close(dm.cpu().numpy()[:n], mm[:n], label + " m")
+            assert_state_close(dv.cpu().numpy()[:n], vv[:n], label + " v")
+        else:
+            assert np.array_equal(bits_of(dm)[:n], mm[:n]) and np.array_equal(bits_of(dv)[:n], vv[:n])
+        for q in range(P):
+            assert np.array_equal(_i8(rq[q]), wq[q]), label + f" replica {q}"
+            assert_bits_equal(rs[q].cpu().numpy(), wsc[q], label + f" replica scales {q}")
+        assert int(words[0:4].view(torch.int32).item()) == flag
+        assert abs(float(words[8:16].view(torch.float64).item()) - ss) <= 1e-9 * ss
+
+
+def test_zpp_sub_ranges_compose_to_the_whole():
+    P, n = 4, 256 * 200 + 99
+    gq, gs, w, m, v = _zpp_problem(P, n, 5)
+    whole = _to_dev(gq, gs, w, m, v, P, n, "f32")
+    a, keep = zdp.make_zpp_args(*whole[:2], *whole[2:5], *whole[5:], n=n, scale=0.25, t=2, **HP)
+    zdp.zdp_step_zpp(a)
+    parts = _to_dev(gq, gs, w, m, v, P, n, "f32")
+    keeps = []
+    for lo, hi in ((0, 256 * 17), (256 * 17, 256 * 100), (256 * 100, n)):
+        g = [x[lo:hi] for x in parts[0]]
+        s_ = [x[lo // 256:] for x in parts[1]]
+        b, k = zdp.make_zpp_args(g, s_, *parts[2:5], *parts[5:], n=n, scale=0.25, t=2, off=lo,
+                                 length=hi - lo, **HP)
+        keeps.append((b, k))
+        zdp.zdp_step_zpp(b)
+    torch.cuda.synchronize()
+    assert_bits_equal(parts[2].cpu().numpy(), whole[2].cpu().numpy(), "master")
+    for q in range(P):
+        assert np.array_equal(_i8(parts[5][q]), _i8(whole[5][q]))
+        assert_bits_equal(parts[6][q].cpu().numpy(), whole[6][q].cpu().numpy(), "scales")
+
+
+def test_zpp_on_the_1p3b_model_sampled_blocks():
+    wl = workloads.gpt_1p3b()
+    P, n, seed = wl.P, wl.n, 9
+    S = -(-n // P)
+    nb = -(-n // 256)
+    gq, gs = [], []
+    for q in range(P):
+        g = workloads.fill_grads(torch.empty(n, dtype=torch.bfloat16, device=DEV), wl, q, 0, seed)
+        qq = torch.empty(n, dtype=torch.int8, device=DEV)
+        sc = torch.empty(nb, dtype=torch.float32, device=DEV)
+        zdp.zdp_quantize_blocks(g, zdp.ZDP_BF16, n, qq, sc)
+        del g
+        gq.append(qq)
+        gs.append(sc)
+    st = torch.empty(3, P * S, dtype=torch.float32, device=DEV)
+    workloads.fill_state(st[0], st[1], st[2], wl, seed)
+    rq = [torch.zeros(n, dtype=torch.int8, device=DEV) for _ in range(P)]
+    rs = [torch.zeros(nb, dtype=torch.float32, device=DEV) for _ in range(P)]
+    rng = np.random.default_rng(seed)
+    blocks = sorted(set(rng.integers(0, nb, 300).tolist()) | {0, nb - 1} |
+                    {(r * S) // 256 for r in range(1, P)})
+    before = {b: [st[k, b * 256:min(n, b * 256 + 256)].cpu().numpy().copy() for k in range(3)]
+              for b in blocks}
+    a, keep = zdp.make_zpp_args(gq, gs, st[0], st[1], st[2], rq, rs, n=n, scale=wl.scale, t=1,
+                                **HP)
+    zdp.zdp_step_zpp(a)
+    torch.cuda.synchronize()
+    for b in blocks:
+        lo, hi = b * 256, min(n, b * 256 + 256)
+        g8 = np.stack([_i8(gq[q][lo:hi]) for q in range(P)])
+        g8s = np.stack([gs[q][b:b + 1].cpu().numpy() for q in range(P)])
+        w, m, v = before[b]
+        wq, wsc = np.zeros((P, hi - lo), np.int8), np.zeros((P, 1), np.float32)
+        oracle.step_zpp(g8, g8s, w, m, v, wq, wsc, n, lo, hi - lo, wl.scale, t=1, base=lo, **HP)
+        assert_state_close(st[0, lo:hi].cpu().numpy(), w, f"block {b} master")
+        assert_state_close(st[1, lo:hi].cpu().numpy(), m, f"block {b} m")
+        for q in (0, P - 1):
+            assert np.array_equal(_i8(rq[q][lo:hi]), wq[q]), f"block {b} replica {q}"
+            assert rs[q][b].item() == wsc[q, 0]

@@ -12,25 +12,25 @@ cudaError_t launch_fused_fp16(const KParams& p, bool vec, int num_sms, cudaStrea
 cudaError_t launch_reduce_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 cudaError_t launch_reduce_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
+int resident_blocks(const void* kernel) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> resident;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = resident.find(kernel);
+  if (it != resident.end()) return it->second;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
+      occ < 1) {
+    occ = 1;
+  }
+  resident[kernel] = occ;
+  return occ;
+}
+
 int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms, int cap) {
   const int64_t work = vec ? (p.hi + kVec - 1) / kVec - p.lo / kVec : p.hi - p.lo;
   if (work <= 0) return 0;
-  static std::mutex mu;
-  static std::unordered_map<const void*, int> resident;
-  int occ = 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = resident.find(kernel);
-    if (it != resident.end()) {
-      occ = it->second;
-    } else {
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess
-          || occ < 1) {
-        occ = 1;
-      }
-      resident[kernel] = occ;
-    }
-  }
+  int occ = resident_blocks(kernel);
   // The caps pay off when every thread walks many vectors; a launch too
   // small to give each capped thread two of them is latency-bound and runs
   // at full occupancy instead (tiny step: 14.4 against 16.2 us).

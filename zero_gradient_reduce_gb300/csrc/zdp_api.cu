@@ -422,4 +422,103 @@ int zdp_step_ring(const zdp_step_args* a, void* stream) {
   return ok();
 }
 
+int zdp_quantize_blocks(const void* x, int xdt, int64_t n, int8_t* q, float* scales,
+                        void* stream) {
+  if (n < 1) return fail(ZDP_ERR_INVALID, "n=%lld must be >= 1", static_cast<long long>(n));
+  if (xdt != ZDP_BF16 && xdt != ZDP_FP16 && xdt != ZDP_F32)
+    return fail(ZDP_ERR_INVALID, "bad input type %d", xdt);
+  if (!x || !q || !scales) return fail(ZDP_ERR_INVALID, "NULL buffer");
+  const int64_t xb = xdt == ZDP_F32 ? 4 : 2;
+  if ((addr(x) & (xb - 1)) != 0 || (addr(scales) & 3u) != 0)
+    return fail(ZDP_ERR_INVALID, "misaligned buffer");
+  std::vector<Range> rs;
+  add_range(rs, x, n * xb, "x", 0);
+  add_range(rs, q, n, "q", 0);
+  add_range(rs, scales, (n + ZDP_QBLOCK - 1) / ZDP_QBLOCK * 4, "scales", 0);
+  if (check_disjoint(rs) != ZDP_OK) return ZDP_ERR_INVALID;
+  int sms = 0;
+  if (num_sms(&sms) != ZDP_OK) return ZDP_ERR_CUDA;
+  cudaError_t e = zdp::launch_quantize(x, xdt, n, q, scales, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return ok();
+}
+
+int zdp_dequantize_blocks(const int8_t* q, const float* scales, int64_t n, uint16_t* out,
+                          void* stream) {
+  if (n < 1) return fail(ZDP_ERR_INVALID, "n=%lld must be >= 1", static_cast<long long>(n));
+  if (!q || !scales || !out) return fail(ZDP_ERR_INVALID, "NULL buffer");
+  if ((addr(out) & 1u) != 0 || (addr(scales) & 3u) != 0)
+    return fail(ZDP_ERR_INVALID, "misaligned buffer");
+  std::vector<Range> rs;
+  add_range(rs, q, n, "q", 0);
+  add_range(rs, scales, (n + ZDP_QBLOCK - 1) / ZDP_QBLOCK * 4, "scales", 0);
+  add_range(rs, out, n * 2, "out", 0);
+  if (check_disjoint(rs) != ZDP_OK) return ZDP_ERR_INVALID;
+  int sms = 0;
+  if (num_sms(&sms) != ZDP_OK) return ZDP_ERR_CUDA;
+  cudaError_t e = zdp::launch_dequantize(q, scales, n, out, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+  return ok();
+}
+
+int zdp_step_zpp(const zdp_zpp_args* a, void* stream) {
+  if (!a) return fail(ZDP_ERR_INVALID, "args is NULL");
+  const int P = a->P;
+  if (!valid_p(P)) return fail(ZDP_ERR_INVALID, "P=%d outside 1..%d", P, ZDP_MAX_P);
+  if (a->n < 1) return fail(ZDP_ERR_INVALID, "n=%lld must be >= 1", static_cast<long long>(a->n));
+  if (a->off < 0 || a->len < 0 || a->off > a->n || a->len > a->n - a->off)
+    return fail(ZDP_ERR_INVALID, "range [%lld, %lld+%lld) outside [0, n=%lld)",
+                static_cast<long long>(a->off), static_cast<long long>(a->off),
+                static_cast<long long>(a->len), static_cast<long long>(a->n));
+  if (a->off % ZDP_QBLOCK != 0 || ((a->off + a->len) % ZDP_QBLOCK != 0 && a->off + a->len != a->n))
+    return fail(ZDP_ERR_INVALID, "the range must start on a %d-element block and end on one or at n",
+                ZDP_QBLOCK);
+  if (a->t < 1) return fail(ZDP_ERR_INVALID, "t=%d must be >= 1", a->t);
+  if (a->moment_dtype != ZDP_MOMENTS_F32 && a->moment_dtype != ZDP_MOMENTS_BF16)
+    return fail(ZDP_ERR_INVALID, "bad moment type %d", a->moment_dtype);
+  if (!a->grads || !a->grad_scales || !a->replicas || !a->replica_scales)
+    return fail(ZDP_ERR_INVALID, "a pointer array is NULL");
+  if (!a->master || !a->m || !a->v) return fail(ZDP_ERR_INVALID, "master, m or v is NULL");
+  if (a->len == 0) return ok();
+  const int64_t n = a->n, len = a->len;
+  const int64_t nb = (n + ZDP_QBLOCK - 1) / ZDP_QBLOCK;
+  const int64_t lb = (len + ZDP_QBLOCK - 1) / ZDP_QBLOCK;
+  const int64_t mbytes = a->moment_dtype == ZDP_MOMENTS_F32 ? 4 : 2;
+  if (!aligned16(a->master) || !aligned16(a->m) || !aligned16(a->v))
+    return fail(ZDP_ERR_INVALID, "master, m and v must be 16-byte aligned");
+  std::vector<Range> outs;
+  add_range(outs, a->master, n * 4, "master", 0);
+  add_range(outs, a->m, n * mbytes, "m", 0);
+  add_range(outs, a->v, n * mbytes, "v", 0);
+  for (int q = 0; q < P; ++q) {
+    if (!a->grads[q] || !a->grad_scales[q] || !a->replicas[q] || !a->replica_scales[q])
+      return fail(ZDP_ERR_INVALID, "a rank-%d pointer is NULL", q);
+    if (!aligned16(a->grads[q]) || !aligned16(a->replicas[q]))
+      return fail(ZDP_ERR_INVALID, "grads[%d] and replicas[%d] must be 16-byte aligned", q, q);
+    if ((addr(a->grad_scales[q]) & 3u) != 0 || (addr(a->replica_scales[q]) & 3u) != 0)
+      return fail(ZDP_ERR_INVALID, "scales of rank %d not 4-byte aligned", q);
+    add_range(outs, a->replicas[q], n, "replicas", q);
+    add_range(outs, a->replica_scales[q], nb * 4, "replica_scales", q);
+  }
+  add_range(outs, a->d_overflow, 4, "d_overflow", 0);
+  add_range(outs, a->d_sumsq, 8, "d_sumsq", 0);
+  if (check_disjoint(outs) != ZDP_OK) return ZDP_ERR_INVALID;
+  for (int q = 0; q < P; ++q) {
+    const Range ins[2] = {{addr(a->grads[q]), addr(a->grads[q]) + static_cast<uintptr_t>(len), "grads", q},
+                          {addr(a->grad_scales[q]),
+                           addr(a->grad_scales[q]) + static_cast<uintptr_t>(lb * 4), "grad_scales", q}};
+    for (const Range& in : ins)
+      for (const Range& o : outs)
+        if (in.lo < o.hi && o.lo < in.hi)
+          return fail(ZDP_ERR_INVALID, "buffers overlap: %s[%d] and %s[%d]", in.what, q, o.what,
+                      o.index);
+  }
+  int sms = 0;
+  if (num_sms(&sms) != ZDP_OK) return ZDP_ERR_CUDA;
+  const zdp::AdamK ad = make_adam(a->lr, a->b1, a->b2, a->eps, a->wd, a->t);
+  cudaError_t e = zdp::launch_zpp(a, ad, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ZeRO++ step launch");
+  return ok();
+}
+
 }  // extern "C"

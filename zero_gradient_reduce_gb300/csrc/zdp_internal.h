@@ -110,8 +110,20 @@ cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t 
 cudaError_t launch_ring(const zdp_step_args* a, const AdamK& ad, float* ws, bool vec, int num_sms,
                         cudaStream_t s);
 
+// ZeRO++ kernels (zdp_zpp.cu).
+cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cudaStream_t s);
+cudaError_t launch_quantize(const void* x, int xdt, int64_t n, int8_t* q, float* scales,
+                            int num_sms, cudaStream_t s);
+cudaError_t launch_dequantize(const int8_t* q, const float* scales, int64_t n, uint16_t* out,
+                              int num_sms, cudaStream_t s);
+
 // Sets this host thread's zdp_last_error() message; returns `code`.
 int report_error(int code, const char* msg);
+
+// Blocks of kThreads threads of `kernel` that fit on one SM (queried once
+// per kernel, then cached).  A persistent grid larger than one wave of them
+// would leave a partial last wave.
+int resident_blocks(const void* kernel);
 
 // Grid size for `kernel` over the elements [p.lo, p.hi): min(resident
 // blocks per SM (queried once per kernel and cached), cap) times num_sms,

@@ -80,16 +80,20 @@ __device__ __forceinline__ bool non_finite(float x) {
 // below 64 * 2^-22 < 1 since i / S < P <= 64, so one correction step lands on
 // the exact floor.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int owner_of(int64_t i, const KParams& p, int P) {
-  int r = static_cast<int>(static_cast<float>(i) * p.inv_s);
+__device__ __forceinline__ int owner_calc(int64_t i, int64_t S, float inv_s, int P) {
+  int r = static_cast<int>(static_cast<float>(i) * inv_s);
   r = r > P - 1 ? P - 1 : r;
-  if (static_cast<int64_t>(r) * p.S > i) {
+  if (static_cast<int64_t>(r) * S > i) {
     --r;
-  } else if (static_cast<int64_t>(r + 1) * p.S <= i) {
+  } else if (static_cast<int64_t>(r + 1) * S <= i) {
     ++r;
   }
   // i < n <= P*S keeps r in [0, P-1]; the clamp makes that hold for any input.
   return r < 0 ? 0 : (r > P - 1 ? P - 1 : r);
+}
+
+__device__ __forceinline__ int owner_of(int64_t i, const KParams& p, int P) {
+  return owner_calc(i, p.S, p.inv_s, P);
 }
 
 // ---------------------------------------------------------------------------
@@ -267,25 +271,25 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[kVec]) {
 // AdamW moments stored as fp32 or bf16 (p.mt is uniform over the grid).  bf16
 // moments are widened exactly and stored rounded to nearest even.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void ld_moments8(const KParams& p, int64_t i0, float (&m)[kVec],
-                                            float (&v)[kVec]) {
-  if (p.mt == ZDP_MOMENTS_F32) {
-    ld_f8(static_cast<const float*>(p.m) + i0, m);
-    ld_f8(static_cast<const float*>(p.v) + i0, v);
+__device__ __forceinline__ void ld_moments8(const void* pm, const void* pv, int mt, int64_t i0,
+                                            float (&m)[kVec], float (&v)[kVec]) {
+  if (mt == ZDP_MOMENTS_F32) {
+    ld_f8(static_cast<const float*>(pm) + i0, m);
+    ld_f8(static_cast<const float*>(pv) + i0, v);
   } else {
-    vec_set<ZDP_BF16>(m, ld16(static_cast<const uint16_t*>(p.m) + i0));
-    vec_set<ZDP_BF16>(v, ld16(static_cast<const uint16_t*>(p.v) + i0));
+    vec_set<ZDP_BF16>(m, ld16(static_cast<const uint16_t*>(pm) + i0));
+    vec_set<ZDP_BF16>(v, ld16(static_cast<const uint16_t*>(pv) + i0));
   }
 }
 
-__device__ __forceinline__ void st_moments8(const KParams& p, int64_t i0, const float (&m)[kVec],
-                                            const float (&v)[kVec]) {
-  if (p.mt == ZDP_MOMENTS_F32) {
-    st_f8(static_cast<float*>(p.m) + i0, m);
-    st_f8(static_cast<float*>(p.v) + i0, v);
+__device__ __forceinline__ void st_moments8(void* pm, void* pv, int mt, int64_t i0,
+                                            const float (&m)[kVec], const float (&v)[kVec]) {
+  if (mt == ZDP_MOMENTS_F32) {
+    st_f8(static_cast<float*>(pm) + i0, m);
+    st_f8(static_cast<float*>(pv) + i0, v);
   } else {
-    st16(static_cast<uint16_t*>(p.m) + i0, pack_bf16x8(m));
-    st16(static_cast<uint16_t*>(p.v) + i0, pack_bf16x8(v));
+    st16(static_cast<uint16_t*>(pm) + i0, pack_bf16x8(m));
+    st16(static_cast<uint16_t*>(pv) + i0, pack_bf16x8(v));
   }
 }
 
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
       if (i0 >= p.lo && i0 + kVec <= p.hi && i0 + kVec <= static_cast<int64_t>(r + 1) * p.S) {
         float w[kVec], m[kVec], v[kVec], g[kVec];
         ld_f8(p.w + i0, w);
-        ld_moments8(p, i0, m, v);
+        ld_moments8(p.m, p.v, p.mt, i0, m, v);
         ring_sum_vec<PT, EXACT, GT>(p, P, r, i0, g);
 #pragma unroll
         for (int k = 0; k < kVec; ++k) g[k] = __fmul_rn(g[k], p.scale);
@@ -446,7 +450,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
 #pragma unroll
         for (int k = 0; k < kVec; ++k) adamw(w[k], m[k], v[k], g[k], p.ad);
         st_f8(p.w + i0, w);
-        st_moments8(p, i0, m, v);
+        st_moments8(p.m, p.v, p.mt, i0, m, v);
         const uint4 b = pack_bf16x8(w);
 #pragma unroll 8
         for (int q = 0; q < P; ++q) st16(p.rep[q] + i0, b);
@@ -522,12 +526,12 @@ __global__ void __launch_bounds__(kThreads) k_adam_gather(const __grid_constant_
       if (i0 >= p.lo && i0 + kVec <= p.hi) {
         float w[kVec], m[kVec], v[kVec], g[kVec];
         ld_f8(p.w + i0, w);
-        ld_moments8(p, i0, m, v);
+        ld_moments8(p.m, p.v, p.mt, i0, m, v);
         ld_f8(p.gin + (i0 - p.gin_base), g);
 #pragma unroll
         for (int k = 0; k < kVec; ++k) adamw(w[k], m[k], v[k], g[k], p.ad);
         st_f8(p.w + i0, w);
-        st_moments8(p, i0, m, v);
+        st_moments8(p.m, p.v, p.mt, i0, m, v);
         if (p.nrep > 0) {
           const uint4 b = pack_bf16x8(w);
           for (int q = 0; q < p.nrep; ++q) st16(p.rep[q] + i0, b);

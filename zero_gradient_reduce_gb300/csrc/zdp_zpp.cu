@@ -1,0 +1,348 @@
+// zdp_zpp.cu -- the ZeRO++ variant of the step (Fudan MLSys ch. 9, 9.4.3):
+// gradients arrive quantized block-wise to int8 for the reduce-scatter, and
+// the all-gather writes int8 replicas of the bf16 parameters.  Blocks are
+// 256 consecutive elements (global index i in block i / 256); a block's scale
+// is max|x| / 127, q = x / scale rounded half to even, clamped to +-127, and
+// an all-zero block has scale 0.  Dequantization is q * scale in fp32.
+//
+// One warp owns one 256-element block at a time (lane l: elements
+// 8l .. 8l+7), so the block maximum needed by the quantizer is one warp
+// reduction; the loops over blocks are warp-uniform.
+#include <algorithm>
+#include <cstring>
+
+#include "zdp_kernels.cuh"
+
+namespace zdp {
+namespace {
+
+constexpr int kQB = ZDP_QBLOCK;  // elements per quantization block (256 = 32 lanes x 8)
+
+struct ZppParams {
+  const int8_t* g[ZDP_MAX_P];   // rank q's int8 gradient of element i: g[q][i - off]
+  const float* gs[ZDP_MAX_P];   // its scales: gs[q][i/256 - off/256]
+  int8_t* rq[ZDP_MAX_P];        // rank q's int8 replica: rq[q][i]
+  float* rs[ZDP_MAX_P];         // its scales: rs[q][i/256]
+  float* w;
+  void* m;
+  void* v;
+  int mt;
+  int64_t n, S, off, lo, hi;
+  float inv_s;
+  int P;
+  float scale;
+  AdamK ad;
+  int32_t* flag;
+  double* sumsq;
+};
+
+__device__ __forceinline__ int zpp_owner(int64_t i, const ZppParams& p) {
+  return owner_calc(i, p.S, p.inv_s, p.P);
+}
+
+__device__ __forceinline__ float dequant(int8_t q, float scale) {
+  return __fmul_rn(__int2float_rn(q), scale);
+}
+
+__device__ __forceinline__ int8_t quant(float x, float scale) {
+  if (scale == 0.0f) return 0;
+  float r = rintf(__fdiv_rn(x, scale));  // round half to even
+  r = fminf(fmaxf(r, -127.0f), 127.0f);
+  return static_cast<int8_t>(__float2int_rn(r));
+}
+
+// Warp maximum of non-negative floats (their bit patterns order like the values).
+__device__ __forceinline__ float warp_absmax(float a) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
+}
+
+__device__ __forceinline__ uint2 pack_i8x8(const int8_t (&q)[kVec]) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    lo |= (static_cast<uint32_t>(static_cast<uint8_t>(q[k])) << (8 * k));
+    hi |= (static_cast<uint32_t>(static_cast<uint8_t>(q[k + 4])) << (8 * k));
+  }
+  return make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ void unpack_i8x8(uint2 u, int8_t (&q)[kVec]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    q[k] = static_cast<int8_t>((u.x >> (8 * k)) & 0xffu);
+    q[k + 4] = static_cast<int8_t>((u.y >> (8 * k)) & 0xffu);
+  }
+}
+
+__device__ __forceinline__ uint2 ld8(const void* ptr) {
+  uint2 x;
+  asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];" : "=r"(x.x), "=r"(x.y) : "l"(ptr));
+  return x;
+}
+__device__ __forceinline__ void st8(void* ptr, uint2 x) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(ptr), "r"(x.x), "r"(x.y) : "memory");
+}
+
+// Ring-order sum of the dequantized gradients of the 8 elements at i0, all
+// owned by r.  PT > 0: P = PT known at compile time (P <= 8).
+template <int PT>
+__device__ __forceinline__ void zpp_ring_vec(const ZppParams& p, int P, int r, int64_t i0,
+                                             int64_t blk, float (&acc)[kVec]) {
+  int q = ring_next(r, P);
+  constexpr int U = PT > 0 ? PT : 8;
+#pragma unroll 1
+  for (int base = 0; base < P; base += U) {
+    uint2 d[U];
+    float sc[U];
+    const int cnt = P - base < U ? P - base : U;
+    int qq = q;
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      if (PT > 0 || k < cnt) {
+        d[k] = ld8(p.g[qq] + (i0 - p.off));
+        sc[k] = p.gs[qq][blk];
+        qq = ring_next(qq, P);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      if (PT > 0 || k < cnt) {
+        int8_t v8[kVec];
+        unpack_i8x8(d[k], v8);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          const float x = dequant(v8[e], sc[k]);
+          acc[e] = (base == 0 && k == 0) ? x : __fadd_rn(acc[e], x);
+        }
+      }
+    }
+    q = qq;
+  }
+}
+
+#ifndef ZDP_ZPP_MIN_BLOCKS
+#define ZDP_ZPP_MIN_BLOCKS 8  // at most 64 registers: 8 resident blocks (measured best)
+#endif
+
+template <int PT>
+__global__ void __launch_bounds__(kThreads, ZDP_ZPP_MIN_BLOCKS) k_zpp(const __grid_constant__ ZppParams p) {
+  const int P = PT > 0 ? PT : p.P;
+  const bool sq = p.sumsq != nullptr;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  bool bad = false;
+  SumSq ss;
+  const int64_t b0 = p.lo / kQB, b1 = (p.hi + kQB - 1) / kQB;  // p.lo is block aligned
+  for (int64_t b = b0 + warp; b < b1; b += nwarps) {               // warp-uniform
+    const int64_t i0 = b * kQB + lane * kVec;
+    const int64_t gb = b - p.off / kQB;                             // gradient scale index
+    int cnt = static_cast<int>(p.hi - i0);
+    cnt = cnt < 0 ? 0 : (cnt > kVec ? kVec : cnt);
+    float pv[kVec];  // the new bf16 parameters as fp32
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) pv[e] = 0.0f;
+    if (cnt > 0) {
+      const int r = zpp_owner(i0, p);
+      float g[kVec];
+      const bool full = cnt == kVec && i0 + kVec <= static_cast<int64_t>(r + 1) * p.S;
+      if (full) {
+        zpp_ring_vec<PT>(p, P, r, i0, gb, g);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          if (e < cnt) {
+            const int64_t i = i0 + e;
+            int q = ring_next(zpp_owner(i, p), P);
+            float acc = dequant(p.g[q][i - p.off], p.gs[q][gb]);
+            for (int k = 1; k < P; ++k) {
+              q = ring_next(q, P);
+              acc = __fadd_rn(acc, dequant(p.g[q][i - p.off], p.gs[q][gb]));
+            }
+            g[e] = acc;
+          }
+        }
+      }
+      if (full) {
+        float w[kVec], m[kVec], v[kVec];
+        ld_f8(p.w + i0, w);
+        ld_moments8(p.m, p.v, p.mt, i0, m, v);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          g[e] = __fmul_rn(g[e], p.scale);
+          adamw(w[e], m[e], v[e], g[e], p.ad);
+          pv[e] = widen1<ZDP_BF16>(to_bf16(w[e]));
+        }
+        account(g, sq, bad, ss);
+        st_f8(p.w + i0, w);
+        st_moments8(p.m, p.v, p.mt, i0, m, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          if (e < cnt) {
+            const int64_t i = i0 + e;
+            const float ge = __fmul_rn(g[e], p.scale);
+            account1(ge, sq, bad, ss);
+            float w = p.w[i], m = ld_moment(p.m, i, p.mt), v = ld_moment(p.v, i, p.mt);
+            adamw(w, m, v, ge, p.ad);
+            p.w[i] = w;
+            st_moment(p.m, i, p.mt, m);
+            st_moment(p.v, i, p.mt, v);
+            pv[e] = widen1<ZDP_BF16>(to_bf16(w));
+          }
+        }
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) amax = fmaxf(amax, fabsf(pv[e]));
+    amax = warp_absmax(amax);
+    const float sc = __fdiv_rn(amax, 127.0f);
+    int8_t qv[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) qv[e] = quant(pv[e], sc);
+    if (cnt == kVec) {
+      const uint2 packed = pack_i8x8(qv);
+      for (int q = 0; q < P; ++q) st8(p.rq[q] + i0, packed);
+    } else {
+      for (int q = 0; q < P; ++q) {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+          if (e < cnt) p.rq[q][i0 + e] = qv[e];
+      }
+    }
+    if (lane == 0)
+      for (int q = 0; q < P; ++q) p.rs[q][b] = sc;
+  }
+  publish_to(p.flag, p.sumsq, bad, ss);
+}
+
+// Block quantization of a bf16 / fp16 / fp32 array (the producer's side).
+template <int XT>  // 0 bf16, 1 fp16, 2 fp32
+__global__ void __launch_bounds__(kThreads) k_quantize(const void* x, int64_t n, int8_t* q,
+                                                       float* scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  for (int64_t b = warp; b * kQB < n; b += nwarps) {
+    const int64_t i0 = b * kQB + lane * kVec;
+    float v[kVec];
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      const int64_t i = i0 + e;
+      float xv = 0.0f;
+      if (i < n) {
+        if constexpr (XT == 0) {
+          xv = widen1<ZDP_BF16>(static_cast<const uint16_t*>(x)[i]);
+        } else if constexpr (XT == 1) {
+          xv = widen1<ZDP_FP16>(static_cast<const uint16_t*>(x)[i]);
+        } else {
+          xv = static_cast<const float*>(x)[i];
+        }
+      }
+      v[e] = xv;
+      amax = fmaxf(amax, fabsf(xv));
+    }
+    amax = warp_absmax(amax);
+    const float sc = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e)
+      if (i0 + e < n) q[i0 + e] = quant(v[e], sc);
+    if (lane == 0) scales[b] = sc;
+  }
+}
+
+// Dequantization back to bf16 (the receiver's side): bf16(q * scale).
+__global__ void __launch_bounds__(kThreads) k_dequantize(const int8_t* q, const float* scales,
+                                                         int64_t n, uint16_t* out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    out[i] = to_bf16(dequant(q[i], scales[i / kQB]));
+}
+
+#ifndef ZDP_CAP_ZPP
+#define ZDP_CAP_ZPP 8
+#endif
+
+// One wave of at most `cap` resident blocks per SM, capped by the work (one
+// warp per 256-element block).
+int grid_warps(const void* kernel, int64_t warps_needed, int num_sms, int cap) {
+  const int64_t blocks = (warps_needed * 32 + kThreads - 1) / kThreads;
+  const int res = resident_blocks(kernel);
+  const int64_t full = static_cast<int64_t>(num_sms) * (res < cap ? res : cap);
+  return static_cast<int>(std::max<int64_t>(1, std::min(blocks, full)));
+}
+
+}  // namespace
+
+cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cudaStream_t s) {
+  ZppParams p;
+  std::memset(&p, 0, sizeof p);
+  const int P = a->P;
+  for (int q = 0; q < P; ++q) {
+    p.g[q] = a->grads[q];
+    p.gs[q] = a->grad_scales[q];
+    p.rq[q] = a->replicas[q];
+    p.rs[q] = a->replica_scales[q];
+  }
+  p.w = a->master;
+  p.m = a->m;
+  p.v = a->v;
+  p.mt = a->moment_dtype;
+  p.n = a->n;
+  p.S = (a->n + P - 1) / P;
+  p.inv_s = 1.0f / static_cast<float>(p.S);
+  p.off = a->off;
+  p.lo = a->off;
+  p.hi = a->off + a->len;
+  p.P = P;
+  p.scale = a->scale;
+  p.ad = ad;
+  p.flag = a->d_overflow;
+  p.sumsq = a->d_sumsq;
+  const int64_t blocks = (a->len + kQB - 1) / kQB;
+  if (blocks == 0) return cudaSuccess;
+  const void* fn;
+  switch (P) {
+    case 1: fn = reinterpret_cast<const void*>(&k_zpp<1>); break;
+    case 2: fn = reinterpret_cast<const void*>(&k_zpp<2>); break;
+    case 3: fn = reinterpret_cast<const void*>(&k_zpp<3>); break;
+    case 4: fn = reinterpret_cast<const void*>(&k_zpp<4>); break;
+    case 5: fn = reinterpret_cast<const void*>(&k_zpp<5>); break;
+    case 6: fn = reinterpret_cast<const void*>(&k_zpp<6>); break;
+    case 7: fn = reinterpret_cast<const void*>(&k_zpp<7>); break;
+    case 8: fn = reinterpret_cast<const void*>(&k_zpp<8>); break;
+    default: fn = reinterpret_cast<const void*>(&k_zpp<0>); break;
+  }
+  void* args[] = {&p};
+  return cudaLaunchKernel(fn, dim3(grid_warps(fn, blocks, num_sms, ZDP_CAP_ZPP)), dim3(kThreads),
+                          args, 0, s);
+}
+
+cudaError_t launch_quantize(const void* x, int xdt, int64_t n, int8_t* q, float* scales,
+                            int num_sms, cudaStream_t s) {
+  const int64_t blocks = (n + kQB - 1) / kQB;
+  const void* fn = xdt == 0   ? reinterpret_cast<const void*>(&k_quantize<0>)
+                   : xdt == 1 ? reinterpret_cast<const void*>(&k_quantize<1>)
+                              : reinterpret_cast<const void*>(&k_quantize<2>);
+  const int grid = grid_warps(fn, blocks, num_sms, 8);
+  if (xdt == 0) {
+    k_quantize<0><<<grid, kThreads, 0, s>>>(x, n, q, scales);
+  } else if (xdt == 1) {
+    k_quantize<1><<<grid, kThreads, 0, s>>>(x, n, q, scales);
+  } else {
+    k_quantize<2><<<grid, kThreads, 0, s>>>(x, n, q, scales);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const int8_t* q, const float* scales, int64_t n, uint16_t* out,
+                              int num_sms, cudaStream_t s) {
+  const int64_t need = (n + kThreads - 1) / kThreads;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, num_sms * 8)));
+  k_dequantize<<<grid, kThreads, 0, s>>>(q, scales, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace zdp

@@ -21,14 +21,17 @@ ZDP_ERR_CUDA = -2
 ZDP_MAX_P = 64
 ZDP_BF16 = 0
 ZDP_FP16 = 1
+ZDP_F32 = 2
 ZDP_MOMENTS_F32 = 0
 ZDP_MOMENTS_BF16 = 1
+ZDP_QBLOCK = 256
 ZDP_NOALLOC_MAX_LEN = 16_777_216
 
 EXPORTS = (
     "zdp_version", "zdp_shard_size", "zdp_reduce_scatter", "zdp_adamw_shard",
     "zdp_all_gather", "zdp_step_workspace_bytes", "zdp_step", "zdp_step_noalloc",
-    "zdp_step_ring_workspace_bytes", "zdp_step_ring", "zdp_last_error",
+    "zdp_step_ring_workspace_bytes", "zdp_step_ring", "zdp_quantize_blocks",
+    "zdp_dequantize_blocks", "zdp_step_zpp", "zdp_last_error",
 )
 
 
@@ -64,6 +67,32 @@ class zdp_step_args(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("moment_dtype", ctypes.c_int),
+    ]
+
+
+class zdp_zpp_args(ctypes.Structure):
+    _fields_ = [
+        ("grads", ctypes.c_void_p),
+        ("grad_scales", ctypes.c_void_p),
+        ("master", ctypes.c_void_p),
+        ("m", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("moment_dtype", ctypes.c_int),
+        ("replicas", ctypes.c_void_p),
+        ("replica_scales", ctypes.c_void_p),
+        ("n", ctypes.c_int64),
+        ("off", ctypes.c_int64),
+        ("len", ctypes.c_int64),
+        ("P", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("lr", ctypes.c_float),
+        ("b1", ctypes.c_float),
+        ("b2", ctypes.c_float),
+        ("eps", ctypes.c_float),
+        ("wd", ctypes.c_float),
+        ("t", ctypes.c_int),
+        ("d_overflow", ctypes.c_void_p),
+        ("d_sumsq", ctypes.c_void_p),
     ]
 
 
@@ -108,6 +137,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.zdp_step_ring_workspace_bytes.argtypes = [ctypes.POINTER(zdp_step_args)]
     lib.zdp_step_ring.restype = ci
     lib.zdp_step_ring.argtypes = [ctypes.POINTER(zdp_step_args), vp]
+    lib.zdp_quantize_blocks.restype = ci
+    lib.zdp_quantize_blocks.argtypes = [vp, ci, i64, vp, vp, vp]
+    lib.zdp_dequantize_blocks.restype = ci
+    lib.zdp_dequantize_blocks.argtypes = [vp, vp, i64, vp, vp]
+    lib.zdp_step_zpp.restype = ci
+    lib.zdp_step_zpp.argtypes = [ctypes.POINTER(zdp_zpp_args), vp]
     lib.zdp_step_noalloc.restype = ci
     lib.zdp_step_noalloc.argtypes = [ctypes.POINTER(zdp_step_args), vp]
     lib.zdp_last_error.restype = ctypes.c_char_p
@@ -253,3 +288,37 @@ def zdp_step_noalloc(args: zdp_step_args, stream=None) -> None:
     """The overflow-checked step with the library's own static scratch (no
     workspace, no allocation); len must not exceed ZDP_NOALLOC_MAX_LEN."""
     _check(load().zdp_step_noalloc(ctypes.byref(args), _stream(stream)))
+
+
+def zdp_quantize_blocks(x: Ptr, xdt: int, n: int, q: Ptr, scales: Ptr, stream=None) -> None:
+    """Block int8 quantization (blocks of 256) of n bf16/fp16/fp32 values."""
+    _check(load().zdp_quantize_blocks(_addr(x), xdt, n, _addr(q), _addr(scales), _stream(stream)))
+
+
+def zdp_dequantize_blocks(q: Ptr, scales: Ptr, n: int, out: Ptr, stream=None) -> None:
+    _check(load().zdp_dequantize_blocks(_addr(q), _addr(scales), n, _addr(out), _stream(stream)))
+
+
+def make_zpp_args(grads: Sequence[Ptr], grad_scales: Sequence[Ptr], master: Ptr, m: Ptr, v: Ptr,
+                  replicas: Sequence[Ptr], replica_scales: Sequence[Ptr], n: int, scale: float,
+                  lr: float, b1: float, b2: float, eps: float, wd: float, t: int, off: int = 0,
+                  length: Optional[int] = None, d_overflow: Ptr = None, d_sumsq: Ptr = None,
+                  moments: str = "f32"):
+    """Builds a zdp_zpp_args; returns (args, keepalive) as make_step_args."""
+    arrs = [_ptr_array(x) for x in (grads, grad_scales, replicas, replica_scales)]
+    a = zdp_zpp_args()
+    a.grads, a.grad_scales, a.replicas, a.replica_scales = [
+        ctypes.cast(x, ctypes.c_void_p) for x in arrs]
+    a.master, a.m, a.v = _addr(master), _addr(m), _addr(v)
+    a.moment_dtype = {"f32": ZDP_MOMENTS_F32, "bf16": ZDP_MOMENTS_BF16}[moments]
+    a.n, a.off = n, off
+    a.len = (n - off) if length is None else length
+    a.P = len(grads)
+    a.scale, a.lr, a.b1, a.b2, a.eps, a.wd, a.t = scale, lr, b1, b2, eps, wd, t
+    a.d_overflow, a.d_sumsq = _addr(d_overflow), _addr(d_sumsq)
+    return a, arrs
+
+
+def zdp_step_zpp(args: zdp_zpp_args, stream=None) -> None:
+    """The ZeRO++ step: int8-block gradients in, int8-block replicas out."""
+    _check(load().zdp_step_zpp(ctypes.byref(args), _stream(stream)))
