@@ -55,6 +55,27 @@ def test_worked_example_with_a_tie(ora):
     assert q[:3].tolist() == [127, 64, -32]
 
 
+def test_ties_on_an_even_base_round_down(ora):
+    # 63.5 -> 64 above is the same under ties-to-even and ties-away; these
+    # fp32 inputs divide by fl(1/127) to exactly k + 0.5 with k even, where
+    # half-to-even keeps k and half-away would give k + 1 (in magnitude).
+    sc = np.float32(1.0) / np.float32(127.0)
+    bits = {62.5: 1056700400, 2.5: 1017201285, 0.5: 998310404, 126.5: 1065287164,
+            10.5: 1034506917}
+    x = np.zeros(256, np.float32)
+    x[0] = 1.0
+    for k, (tie, b) in enumerate(bits.items()):
+        val = np.array([b], np.uint32).view(np.float32)[0]
+        assert val / sc == np.float32(tie)  # the premise: an exact tie
+        x[1 + 2 * k], x[2 + 2 * k] = val, -val
+    q, s = ora.quantize_blocks(x)
+    assert s[0] == sc
+    want = [127]
+    for tie in bits:
+        want += [int(tie - 0.5), -int(tie - 0.5)]
+    assert q[:len(want)].tolist() == want
+
+
 def test_zpp_step_equals_bf16_step_when_dequantization_is_exact(ora):
     P, n = 4, 256 * 20 + 37
     rng = np.random.default_rng(2)
