@@ -94,9 +94,21 @@ MUTANTS = [
     ("sum of |g| instead of g^2",
      [(CPP, "ss += static_cast<double>(g[j]) * static_cast<double>(g[j]);",
        "ss += std::fabs(static_cast<double>(g[j]));")]),
+    ("sum of squares in fp32",
+     [(CPP, "ss += static_cast<double>(g[j]) * static_cast<double>(g[j]);",
+       "ss += static_cast<double>(g[j] * g[j]);")]),
     ("sum of squares taken before the scale",
      [(CPP, "ss += static_cast<double>(g[j]) * static_cast<double>(g[j]);",
        "ss += static_cast<double>(g[j] / scale) * static_cast<double>(g[j] / scale);")]),
+    ("reduce-scatter sums |g|",
+     [(CPP, "ss += static_cast<double>(g) * static_cast<double>(g);\n    shards[i] = g;",
+       "ss += std::fabs(static_cast<double>(g));\n    shards[i] = g;")]),
+    ("ZeRO++ sum of squares in fp32",
+     [(CPP, "ss += static_cast<double>(g) * static_cast<double>(g);\n    const int64_t k = i - base;",
+       "ss += static_cast<double>(g * g);\n    const int64_t k = i - base;")]),
+    ("ZeRO++ sum of squares skips the owner's rank",
+     [(CPP, "vals[q] = dequant_one(gq[q * ld + j], gs[q * sld + i / kQBlock - off / kQBlock]);",
+       "vals[q] = q == owner_of(i, S) ? 0.0f : dequant_one(gq[q * ld + j], gs[q * sld + i / kQBlock - off / kQBlock]);")]),
     # replicas
     ("replicas truncated to bf16",
      [(CPP, "const uint16_t p = float_to_bf16_rne(master[k]);",
