@@ -46,6 +46,43 @@ def test_quantize_and_dequantize_match_the_oracle(n):
         assert np.array_equal(bits_of(out), want)
 
 
+def test_quantizer_near_ties_match_the_oracle():
+    # Values within a few ulps of (k + 1/2) * scale, for every k and several
+    # block maxima: the quotient lands on or next to a rounding tie.
+    rng = np.random.default_rng(7)
+    blocks = []
+    for amax in [1.0, 3.0e-3, 0.7071, 123.456, 2.0 ** -60, 6.1e4]:
+        a = np.float32(amax)
+        sc = a / np.float32(127.0)
+        centers = (np.arange(-127, 127, dtype=np.float32) + np.float32(0.5)) * sc
+        vals = [centers]
+        up, dn = centers.copy(), centers.copy()
+        for _ in range(3):
+            up = np.nextafter(up, np.float32(np.inf))
+            dn = np.nextafter(dn, np.float32(-np.inf))
+            vals += [up, dn]
+        v = np.concatenate(vals)
+        v = v[np.abs(v) <= a]
+        rng.shuffle(v)
+        for lo in range(0, v.size, 255):
+            blk = np.zeros(256, np.float32)
+            chunk = v[lo:lo + 255]
+            blk[1:1 + chunk.size] = chunk
+            blk[0] = a  # fixes the block maximum, hence the scale
+            blocks.append(blk)
+    x = np.concatenate(blocks)
+    n = x.size
+    q = torch.empty(n, dtype=torch.int8, device=DEV)
+    sc = torch.empty(n // 256, dtype=torch.float32, device=DEV)
+    zdp.zdp_quantize_blocks(torch.from_numpy(x).to(DEV), zdp.ZDP_F32, n, q, sc)
+    wq, ws = oracle.quantize_blocks(x)
+    torch.cuda.synchronize()
+    assert_bits_equal(sc.cpu().numpy(), ws, "scales")
+    got = _i8(q)
+    bad = np.nonzero(got != wq)[0]
+    assert bad.size == 0, f"{bad.size} codes differ, first at {bad[:4]}: {got[bad[:4]]} vs {wq[bad[:4]]}"
+
+
 def _zpp_problem(P, n, seed, moments="f32"):
     rng = np.random.default_rng(seed)
     x = (rng.standard_normal((P, n)) * 1e-3 * 10.0 ** rng.uniform(-1, 1, (P, 1))).astype(np.float32)
@@ -79,7 +116,7 @@ def _to_dev(gq, gs, w, m, v, P, n, moments):
     return dg, ds, dw, dm, dv, rq, rs
 
 
-@pytest.mark.parametrize("P", [1, 2, 3, 8, 12, 16])
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 8, 12, 16, 32, 64])
 @pytest.mark.parametrize("moments", ["f32", "bf16"])
 def test_zpp_step_matches_the_oracle(P, moments):
     for n in sorted({256 * P * 3 + 7, 40_000 + P, 256 * 64}):

@@ -44,11 +44,44 @@ __device__ __forceinline__ float dequant(int8_t q, float scale) {
   return __fmul_rn(__int2float_rn(q), scale);
 }
 
-__device__ __forceinline__ int8_t quant(float x, float scale) {
-  if (scale == 0.0f) return 0;
-  float r = rintf(__fdiv_rn(x, scale));  // round half to even
+// Reference form of the code: exact division, round half to even, clamp.
+__device__ __forceinline__ int quant_div(float x, float scale) {
+  float r = rintf(__fdiv_rn(x, scale));
   r = fminf(fmaxf(r, -127.0f), 127.0f);
-  return static_cast<int8_t>(__float2int_rn(r));
+  return __float2int_rn(r);
+}
+
+// The same code from a multiply by rcp = fl(1/scale), without conversion
+// instructions.  Adding 1.5 * 2^23 rounds y to an integer, half to even, and
+// leaves that integer in the low mantissa bits.  Since |x| <= 128 * scale,
+// y = fl(x * rcp) lies within 128 * 2^-23 < 2e-5 of x / scale, and
+// fl(x / scale) within 128 * 2^-24 of it; unless y is within 1e-4 of a
+// half-integer both round to the same integer.  Otherwise (and for NaN) the
+// exact division decides.  The caller guarantees scale != 0 and rcp finite.
+__device__ __forceinline__ int quant_rcp(float x, float scale, float rcp) {
+  const float y = __fmul_rn(x, rcp);
+  const float t = __fadd_rn(y, 12582912.0f);
+  const float d = __fsub_rn(y, __fsub_rn(t, 12582912.0f));  // exact: y minus its rounding
+  if (fabsf(__fsub_rn(fabsf(d), 0.5f)) > 1e-4f) {
+    const int q = __float_as_int(t) - 0x4B400000;
+    return q < -127 ? -127 : (q > 127 ? 127 : q);
+  }
+  return quant_div(x, scale);
+}
+
+// Codes of 8 values sharing one block scale (0 for an all-zero block).
+__device__ __forceinline__ void quant8(const float (&x)[kVec], float scale, int (&q)[kVec]) {
+  const float rcp = __frcp_rn(scale);
+  if (scale == 0.0f) {
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) q[e] = 0;
+  } else if (isfinite(rcp)) {
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) q[e] = quant_rcp(x[e], scale, rcp);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) q[e] = quant_div(x[e], scale);
+  }
 }
 
 // Warp maximum of non-negative floats (their bit patterns order like the values).
@@ -56,22 +89,14 @@ __device__ __forceinline__ float warp_absmax(float a) {
   return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
 }
 
-__device__ __forceinline__ uint2 pack_i8x8(const int8_t (&q)[kVec]) {
+__device__ __forceinline__ uint2 pack_i8x8(const int (&q)[kVec]) {
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    lo |= (static_cast<uint32_t>(static_cast<uint8_t>(q[k])) << (8 * k));
-    hi |= (static_cast<uint32_t>(static_cast<uint8_t>(q[k + 4])) << (8 * k));
+    lo |= (static_cast<uint32_t>(q[k]) & 0xffu) << (8 * k);
+    hi |= (static_cast<uint32_t>(q[k + 4]) & 0xffu) << (8 * k);
   }
   return make_uint2(lo, hi);
-}
-
-__device__ __forceinline__ void unpack_i8x8(uint2 u, int8_t (&q)[kVec]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    q[k] = static_cast<int8_t>((u.x >> (8 * k)) & 0xffu);
-    q[k + 4] = static_cast<int8_t>((u.y >> (8 * k)) & 0xffu);
-  }
 }
 
 __device__ __forceinline__ uint2 ld8(const void* ptr) {
@@ -84,48 +109,60 @@ __device__ __forceinline__ void st8(void* ptr, uint2 x) {
 }
 
 // Ring-order sum of the dequantized gradients of the 8 elements at i0, all
-// owned by r.  PT > 0: P = PT known at compile time (P <= 8).
+// owned by r.  PT > 0: P = PT known at compile time (PT <= 8, or a multiple
+// of 8 taken in exact groups of 8); PT = 0: any P, the last group partial.
 template <int PT>
 __device__ __forceinline__ void zpp_ring_vec(const ZppParams& p, int P, int r, int64_t i0,
                                              int64_t blk, float (&acc)[kVec]) {
   int q = ring_next(r, P);
-  constexpr int U = PT > 0 ? PT : 8;
+  constexpr int U = PT > 0 && PT < 8 ? PT : 8;
+  constexpr bool EXACT = PT > 0;
 #pragma unroll 1
   for (int base = 0; base < P; base += U) {
     uint2 d[U];
     float sc[U];
     const int cnt = P - base < U ? P - base : U;
-    int qq = q;
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-      if (PT > 0 || k < cnt) {
-        d[k] = ld8(p.g[qq] + (i0 - p.off));
-        sc[k] = p.gs[qq][blk];
-        qq = ring_next(qq, P);
+      if (EXACT || k < cnt) {
+        d[k] = ld8(p.g[q] + (i0 - p.off));
+        sc[k] = p.gs[q][blk];
+        q = ring_next(q, P);
       }
     }
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-      if (PT > 0 || k < cnt) {
-        int8_t v8[kVec];
-        unpack_i8x8(d[k], v8);
+      if (EXACT || k < cnt) {
+        float v8[kVec];  // the int8 codes, converted exactly
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v8[e] = __int2float_rn(static_cast<int8_t>((d[k].x >> (8 * e)) & 0xffu));
+          v8[e + 4] = __int2float_rn(static_cast<int8_t>((d[k].y >> (8 * e)) & 0xffu));
+        }
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
-          const float x = dequant(v8[e], sc[k]);
+          const float x = __fmul_rn(v8[e], sc[k]);
           acc[e] = (base == 0 && k == 0) ? x : __fadd_rn(acc[e], x);
         }
       }
     }
-    q = qq;
   }
 }
 
+// Resident blocks the register allocation must allow (measured best on
+// GB300): 8 (64 registers) for P <= 8 and the generic kernel, 6 (80
+// registers) for the exact multiples of 8 above 8, which keep two groups of
+// eight ranks' loads in flight.
 #ifndef ZDP_ZPP_MIN_BLOCKS
-#define ZDP_ZPP_MIN_BLOCKS 8  // at most 64 registers: 8 resident blocks (measured best)
+#define ZDP_ZPP_MIN_BLOCKS 8
+#endif
+#ifndef ZDP_ZPP_MIN_BLOCKS_WIDE
+#define ZDP_ZPP_MIN_BLOCKS_WIDE 6
 #endif
 
 template <int PT>
-__global__ void __launch_bounds__(kThreads, ZDP_ZPP_MIN_BLOCKS) k_zpp(const __grid_constant__ ZppParams p) {
+__global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : ZDP_ZPP_MIN_BLOCKS)
+    k_zpp(const __grid_constant__ ZppParams p) {
   const int P = PT > 0 ? PT : p.P;
   const bool sq = p.sumsq != nullptr;
   const int lane = threadIdx.x & 31;
@@ -171,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, ZDP_ZPP_MIN_BLOCKS) k_zpp(const __gr
         for (int e = 0; e < kVec; ++e) {
           g[e] = __fmul_rn(g[e], p.scale);
           adamw(w[e], m[e], v[e], g[e], p.ad);
-          pv[e] = widen1<ZDP_BF16>(to_bf16(w[e]));
         }
+        vec_set<ZDP_BF16>(pv, pack_bf16x8(w));  // the bf16 parameters, widened
         account(g, sq, bad, ss);
         st_f8(p.w + i0, w);
         st_moments8(p.m, p.v, p.mt, i0, m, v);
@@ -198,9 +235,8 @@ __global__ void __launch_bounds__(kThreads, ZDP_ZPP_MIN_BLOCKS) k_zpp(const __gr
     for (int e = 0; e < kVec; ++e) amax = fmaxf(amax, fabsf(pv[e]));
     amax = warp_absmax(amax);
     const float sc = __fdiv_rn(amax, 127.0f);
-    int8_t qv[kVec];
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) qv[e] = quant(pv[e], sc);
+    int qv[kVec];
+    quant8(pv, sc, qv);
     if (cnt == kVec) {
       const uint2 packed = pack_i8x8(qv);
       for (int q = 0; q < P; ++q) st8(p.rq[q] + i0, packed);
@@ -208,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, ZDP_ZPP_MIN_BLOCKS) k_zpp(const __gr
       for (int q = 0; q < P; ++q) {
 #pragma unroll
         for (int e = 0; e < kVec; ++e)
-          if (e < cnt) p.rq[q][i0 + e] = qv[e];
+          if (e < cnt) p.rq[q][i0 + e] = static_cast<int8_t>(qv[e]);
       }
     }
     if (lane == 0)
@@ -246,9 +282,11 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const void* x, int64_t n,
     }
     amax = warp_absmax(amax);
     const float sc = __fdiv_rn(amax, 127.0f);
+    int qv[kVec];
+    quant8(v, sc, qv);
 #pragma unroll
     for (int e = 0; e < kVec; ++e)
-      if (i0 + e < n) q[i0 + e] = quant(v[e], sc);
+      if (i0 + e < n) q[i0 + e] = static_cast<int8_t>(qv[e]);
     if (lane == 0) scales[b] = sc;
   }
 }
@@ -313,6 +351,9 @@ cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cuda
     case 6: fn = reinterpret_cast<const void*>(&k_zpp<6>); break;
     case 7: fn = reinterpret_cast<const void*>(&k_zpp<7>); break;
     case 8: fn = reinterpret_cast<const void*>(&k_zpp<8>); break;
+    case 16: fn = reinterpret_cast<const void*>(&k_zpp<16>); break;
+    case 32: fn = reinterpret_cast<const void*>(&k_zpp<32>); break;
+    case 64: fn = reinterpret_cast<const void*>(&k_zpp<64>); break;
     default: fn = reinterpret_cast<const void*>(&k_zpp<0>); break;
   }
   void* args[] = {&p};
