@@ -140,29 +140,37 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
 def copy_ceiling_gbs(dev, reps=10):
-    """This run's device-to-device copy ceiling, measured the way the peak in
-    MEASURED_PEAKS.json is: b.copy_(a) over 1 Gi bf16 elements, read + write
-    bytes, best of `reps`, CUDA events.  Returns (best, median) in GB/s."""
+    """This run's device-to-device copy ceilings over 1 Gi bf16 elements, read +
+    write bytes, CUDA events, best and median of `reps`: torch's b.copy_(a)
+    (the way the peak in MEASURED_PEAKS.json was taken) and zdp_copy, the
+    library's plain 16-byte streaming copy (the step's own access pattern)."""
     import torch
+
+    from zero_gradient_reduce_gb300 import zdp
 
     a = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
     b = torch.empty_like(a)
     a.fill_(1.0)
+    nbytes = a.numel() * a.element_size()
     stream = torch.cuda.current_stream(dev)
-    for _ in range(2):
-        b.copy_(a)
-    rates = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        b.copy_(a)
-        e1.record(stream)
-        e1.synchronize()
-        rates.append(2 * a.numel() * a.element_size() / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    out = {}
+    for name, fn in (("torch_copy", lambda: b.copy_(a)),
+                     ("zdp_copy", lambda: zdp.zdp_copy(b, a, nbytes, stream))):
+        for _ in range(2):
+            fn()
+        rates = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            rates.append(2 * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        rates.sort()
+        out[name] = (rates[-1], rates[len(rates) // 2])
     del a, b
     torch.cuda.empty_cache()
-    rates.sort()
-    return rates[-1], rates[len(rates) // 2]
+    return out
 
 
 def kernel_source_hash() -> str:
@@ -385,7 +393,8 @@ def run_ours(args):
             e2e["value"] = whole_job_rate(n, 1, world, slowest * 1e3)
         e2e.pop("seconds_per_step", None)
 
-    copy_best, copy_median = copy_ceiling_gbs(dev)
+    copies = copy_ceiling_gbs(dev)
+    copy_best, copy_median = copies["torch_copy"]
 
     out = None
     if rank == 0:
@@ -426,6 +435,8 @@ def run_ours(args):
                 "copy_ceiling_this_run": copy_best,
                 "copy_ceiling_this_run_median": copy_median,
                 "frac_of_this_run_copy": achieved / copy_best,
+                "zdp_copy_this_run": copies["zdp_copy"][0],
+                "zdp_copy_this_run_median": copies["zdp_copy"][1],
                 "frac_of_nominal_hbm": achieved / NOMINAL_HBM_GBS,
             },
             "gpu_launches": K * launches_per_step,

@@ -281,6 +281,17 @@ int zdp_step_zpp(const zdp_zpp_args* args, void* stream);
  * on two streams without an ordering between them, race on it. */
 int zdp_step_noalloc(const zdp_step_args* args, void* stream);
 
+/* A plain device-to-device copy of `bytes` bytes with 16-byte streaming
+ * loads and stores (ld/st.global.cs) on a persistent grid of 128-thread
+ * blocks: the access pattern of the step's kernels with no arithmetic.  The
+ * pages have no counterpart; it measures the copy ceiling the step is held
+ * against.
+ *   dst, src  device pointers, both 16-byte aligned, not overlapping.
+ *   bytes     a non-negative multiple of 16 (0: nothing is enqueued).
+ * Returns ZDP_ERR_INVALID (nothing enqueued) for a NULL pointer, a size or
+ * alignment outside these rules, or overlapping ranges. */
+int zdp_copy(void* dst, const void* src, int64_t bytes, void* stream);
+
 /* Message for the last non-OK return on this host thread ("" if none). */
 const char* zdp_last_error(void);
 

@@ -169,6 +169,18 @@ def test_zpp_rejects_bad_arguments(lib, mutate, needle):
         zdp.zdp_step_zpp(a, stream=0)
 
 
+def test_copy_rejects_bad_arguments(lib):
+    with pytest.raises(zdp.ZdpError, match="multiple of 16"):
+        zdp.zdp_copy(FAKE, FAKE + 4096, 100, stream=0)
+    with pytest.raises(zdp.ZdpError, match="aligned"):
+        zdp.zdp_copy(FAKE + 8, FAKE + 4096, 256, stream=0)
+    with pytest.raises(zdp.ZdpError, match="overlap"):
+        zdp.zdp_copy(FAKE, FAKE + 64, 256, stream=0)
+    with pytest.raises(zdp.ZdpError, match="NULL"):
+        zdp.zdp_copy(0, FAKE, 256, stream=0)
+    zdp.zdp_copy(FAKE, FAKE, 0, stream=0)  # nothing to do: never reaches CUDA
+
+
 def test_quantizer_rejects_bad_arguments(lib):
     with pytest.raises(zdp.ZdpError, match="input type"):
         zdp.zdp_quantize_blocks(FAKE, 7, 10, FAKE + 4096, FAKE + 8192, stream=0)

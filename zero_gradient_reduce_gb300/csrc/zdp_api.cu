@@ -242,6 +242,25 @@ int zdp_all_gather(const float* master, uint16_t* const* replicas, int64_t n, in
   return ok();
 }
 
+int zdp_copy(void* dst, const void* src, int64_t bytes, void* stream) {
+  if (bytes < 0 || bytes % 16 != 0)
+    return fail(ZDP_ERR_INVALID, "bytes=%lld must be a non-negative multiple of 16",
+                static_cast<long long>(bytes));
+  if (bytes == 0) return ok();
+  if (!dst || !src) return fail(ZDP_ERR_INVALID, "dst or src is NULL");
+  if (!aligned16(dst) || !aligned16(src))
+    return fail(ZDP_ERR_INVALID, "dst and src must be 16-byte aligned");
+  std::vector<Range> rs;
+  add_range(rs, dst, bytes, "dst", 0);
+  add_range(rs, src, bytes, "src", 0);
+  if (check_disjoint(rs) != ZDP_OK) return ZDP_ERR_INVALID;
+  int sms = 0;
+  if (num_sms(&sms) != ZDP_OK) return ZDP_ERR_CUDA;
+  cudaError_t e = zdp::launch_copy(dst, src, bytes, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy launch");
+  return ok();
+}
+
 size_t zdp_step_workspace_bytes(const zdp_step_args* a) {
   if (!a || !a->check_overflow || a->len <= 0) return 0;
   // 256 B for the device flag, then the reduced gradients of the range,

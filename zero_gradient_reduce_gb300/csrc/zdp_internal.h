@@ -114,6 +114,7 @@ cudaError_t launch_ring(const zdp_step_args* a, const AdamK& ad, float* ws, bool
 cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize(const void* x, int xdt, int64_t n, int8_t* q, float* scales,
                             int num_sms, cudaStream_t s);
+cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, int num_sms, cudaStream_t s);
 cudaError_t launch_dequantize(const int8_t* q, const float* scales, int64_t n, uint16_t* out,
                               int num_sms, cudaStream_t s);
 

@@ -31,7 +31,7 @@ EXPORTS = (
     "zdp_version", "zdp_shard_size", "zdp_reduce_scatter", "zdp_adamw_shard",
     "zdp_all_gather", "zdp_step_workspace_bytes", "zdp_step", "zdp_step_noalloc",
     "zdp_step_ring_workspace_bytes", "zdp_step_ring", "zdp_quantize_blocks",
-    "zdp_dequantize_blocks", "zdp_step_zpp", "zdp_last_error",
+    "zdp_dequantize_blocks", "zdp_step_zpp", "zdp_copy", "zdp_last_error",
 )
 
 
@@ -145,6 +145,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.zdp_step_zpp.argtypes = [ctypes.POINTER(zdp_zpp_args), vp]
     lib.zdp_step_noalloc.restype = ci
     lib.zdp_step_noalloc.argtypes = [ctypes.POINTER(zdp_step_args), vp]
+    lib.zdp_copy.restype = ci
+    lib.zdp_copy.argtypes = [vp, vp, ctypes.c_int64, vp]
     lib.zdp_last_error.restype = ctypes.c_char_p
     lib.zdp_last_error.argtypes = []
     _lib = lib
@@ -297,6 +299,11 @@ def zdp_quantize_blocks(x: Ptr, xdt: int, n: int, q: Ptr, scales: Ptr, stream=No
 
 def zdp_dequantize_blocks(q: Ptr, scales: Ptr, n: int, out: Ptr, stream=None) -> None:
     _check(load().zdp_dequantize_blocks(_addr(q), _addr(scales), n, _addr(out), _stream(stream)))
+
+
+def zdp_copy(dst: Ptr, src: Ptr, nbytes: int, stream=None) -> None:
+    """Plain 16-byte streaming device copy (the copy-ceiling probe)."""
+    _check(load().zdp_copy(_addr(dst), _addr(src), nbytes, _stream(stream)))
 
 
 def make_zpp_args(grads: Sequence[Ptr], grad_scales: Sequence[Ptr], master: Ptr, m: Ptr, v: Ptr,
