@@ -7,8 +7,10 @@
 
 namespace zdp {
 
-cudaError_t launch_fused_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
-cudaError_t launch_fused_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_fused_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s,
+                              bool overlap_prev);
+cudaError_t launch_fused_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s,
+                              bool overlap_prev);
 cudaError_t launch_reduce_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 cudaError_t launch_reduce_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
@@ -51,9 +53,10 @@ cudaError_t launch_fn(const void* fn, const KParams& p, bool vec, int num_sms, i
 }
 }  // namespace
 
-cudaError_t launch_fused(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s) {
-  return gdt == ZDP_BF16 ? launch_fused_bf16(p, vec, num_sms, s)
-                         : launch_fused_fp16(p, vec, num_sms, s);
+cudaError_t launch_fused(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s,
+                         bool overlap_prev) {
+  return gdt == ZDP_BF16 ? launch_fused_bf16(p, vec, num_sms, s, overlap_prev)
+                         : launch_fused_fp16(p, vec, num_sms, s, overlap_prev);
 }
 
 cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s) {

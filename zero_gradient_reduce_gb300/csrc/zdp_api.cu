@@ -379,7 +379,7 @@ int zdp_step(const zdp_step_args* a, void* stream) {
     for (int64_t lo = off; lo < off + len; lo += bucket) {
       p.lo = lo;
       p.hi = std::min(off + len, lo + bucket);
-      cudaError_t e = zdp::launch_fused(p, a->gdt, vec, sms, s);
+      cudaError_t e = zdp::launch_fused(p, a->gdt, vec, sms, s, lo != off);
       if (e != cudaSuccess) return cuda_fail(e, "fused step launch");
     }
     return ok();

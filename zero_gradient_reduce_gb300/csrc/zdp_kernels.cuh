@@ -434,9 +434,30 @@ __device__ __forceinline__ void fused_elem(const KParams& p, int P, int64_t i, b
   for (int q = 0; q < P; ++q) p.rep[q][i] = b;
 }
 
+#ifndef ZDP_PDL
+#define ZDP_PDL 1
+#endif
+
+// Programmatic dependent launch between consecutive k_fused launches of one
+// call (disjoint bucket ranges): every block lets the next launch begin as
+// soon as it starts, and waits for the previous launch to complete before it
+// exits, so a launch completes only after all earlier ones.  Both are no-ops
+// for a launch made without programmatic stream serialization.
+__device__ __forceinline__ void allow_next_launch() {
+#if ZDP_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void wait_previous_launch() {
+#if ZDP_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
 // Reduce-scatter + AdamW + cast + all-gather in one pass.
 template <int PT, bool EXACT, int GT, bool VEC>
 __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KParams p) {
+  allow_next_launch();
   const int P = ranks<PT, EXACT>(p);
   const bool sq = p.sumsq != nullptr;
   bool bad = false;
@@ -474,6 +495,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
     for (int64_t i = p.lo + tid; i < p.hi; i += stride) fused_elem<GT>(p, P, i, sq, bad, ss);
   }
   publish(p, bad, ss);
+  wait_previous_launch();
 }
 
 // Reduce-scatter only: reduced gradients to gout.
