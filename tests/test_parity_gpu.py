@@ -261,6 +261,26 @@ def test_checked_step_without_overflow_matches_single_pass():
     assert_bits_equal(a.replica_bits(), b.replica_bits(), "replicas")
 
 
+@pytest.mark.parametrize("bucket", [1000, 4099, 30_000])
+@pytest.mark.parametrize("inject_at", [None, 5, 99_990])
+def test_bucketed_checked_step_matches_oracle(bucket, inject_at):
+    # Consecutive bucket launches of one call overlap (programmatic dependent
+    # launch); the gated update must still see the flag of every bucket's
+    # reduce pass, including an infinity in the first or the last bucket.
+    P, n = 8, 100_003
+    gbits, w, m, v = random_problem(P, n, 21, oracle.FP16)
+    if inject_at is not None:
+        gbits[3, inject_at] = 0x7C00  # +inf in fp16
+    rep = np.full((P, n), 0x3F80, np.uint16)
+    dev = DeviceStep(P, n, torch.float16)
+    dev.load(gbits, w, m, v, rep)
+    scale = 1.0 / (P * 65536.0)
+    dev.step(scale, 7, check_overflow=True, bucket_elems=bucket)
+    flag, ss = _oracle_step(gbits, w, m, v, rep, n, scale, 7, oracle.FP16, check=True)
+    assert flag == (0 if inject_at is None else 1)
+    _compare_step(dev, w, m, v, rep, flag, ss, f"bucketed checked {bucket} {inject_at}")
+
+
 def test_finite_gradients_overflowing_fp32():
     P, n = 2, 4096
     gbits, w, m, v = random_problem(P, n, 12)

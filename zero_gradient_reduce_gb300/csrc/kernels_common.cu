@@ -11,8 +11,10 @@ cudaError_t launch_fused_bf16(const KParams& p, bool vec, int num_sms, cudaStrea
                               bool overlap_prev);
 cudaError_t launch_fused_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s,
                               bool overlap_prev);
-cudaError_t launch_reduce_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
-cudaError_t launch_reduce_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_reduce_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s,
+                               bool overlap_prev);
+cudaError_t launch_reduce_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s,
+                               bool overlap_prev);
 
 int resident_blocks(const void* kernel) {
   static std::mutex mu;
@@ -43,13 +45,29 @@ int grid_for(const void* kernel, const KParams& p, bool vec, int num_sms, int ca
   return static_cast<int>(need < full ? need : full);
 }
 
+cudaError_t launch_kernel(const void* fn, int grid, void** args, cudaStream_t s,
+                          bool overlap_prev) {
+  if (!ZDP_PDL || !overlap_prev) return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 namespace {
 cudaError_t launch_fn(const void* fn, const KParams& p, bool vec, int num_sms, int cap,
-                      cudaStream_t s) {
+                      cudaStream_t s, bool overlap_prev = false) {
   const int grid = grid_for(fn, p, vec, num_sms, cap);
   if (grid == 0) return cudaSuccess;
   void* args[] = {const_cast<KParams*>(&p)};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, s);
+  return launch_kernel(fn, grid, args, s, overlap_prev);
 }
 }  // namespace
 
@@ -59,17 +77,19 @@ cudaError_t launch_fused(const KParams& p, int gdt, bool vec, int num_sms, cudaS
                          : launch_fused_fp16(p, vec, num_sms, s, overlap_prev);
 }
 
-cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s) {
-  return gdt == ZDP_BF16 ? launch_reduce_bf16(p, vec, num_sms, s)
-                         : launch_reduce_fp16(p, vec, num_sms, s);
+cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s,
+                          bool overlap_prev) {
+  return gdt == ZDP_BF16 ? launch_reduce_bf16(p, vec, num_sms, s, overlap_prev)
+                         : launch_reduce_fp16(p, vec, num_sms, s, overlap_prev);
 }
 
-cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
+cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s,
+                               bool overlap_prev) {
   const void* fn = vec ? reinterpret_cast<const void*>(&k_adam_gather<true>)
                        : reinterpret_cast<const void*>(&k_adam_gather<false>);
   const int cap = p.nrep == 0 ? ZDP_CAP_ADAM
                   : (p.mt == ZDP_MOMENTS_F32 ? ZDP_CAP_ADAM_GATHER : ZDP_CAP_ADAM_GATHER_BF16M);
-  return launch_fn(fn, p, vec, num_sms, cap, s);
+  return launch_fn(fn, p, vec, num_sms, cap, s, overlap_prev);
 }
 
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {

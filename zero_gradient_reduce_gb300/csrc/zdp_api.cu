@@ -398,7 +398,7 @@ int zdp_step(const zdp_step_args* a, void* stream) {
   for (int64_t lo = off; lo < off + len; lo += bucket) {
     p.lo = lo;
     p.hi = std::min(off + len, lo + bucket);
-    e = zdp::launch_reduce(p, a->gdt, vec, sms, s);
+    e = zdp::launch_reduce(p, a->gdt, vec, sms, s, lo != off);
     if (e != cudaSuccess) return cuda_fail(e, "reduce pass launch");
   }
   p.gout = nullptr;
@@ -410,7 +410,7 @@ int zdp_step(const zdp_step_args* a, void* stream) {
   for (int64_t lo = off; lo < off + len; lo += bucket) {
     p.lo = lo;
     p.hi = std::min(off + len, lo + bucket);
-    e = zdp::launch_adam_gather(p, vec, sms, s);
+    e = zdp::launch_adam_gather(p, vec, sms, s, lo != off);
     if (e != cudaSuccess) return cuda_fail(e, "update pass launch");
   }
   return ok();

@@ -101,13 +101,18 @@ struct KParams {
 // per SM, capped by the work.  Each returns the launch status.
 // The fused and reduce kernels add the sum of squares when p.sumsq is set.
 // overlap_prev: launch with programmatic stream serialization, so that the
-// blocks of this launch may start while the previous launch on the stream (a
-// k_fused launch over a disjoint range) drains; k_fused waits for it before
-// exiting, so stream order still holds for whatever follows.
+// blocks of this launch may start while the previous launch on the stream
+// (a launch of the same kernel over a disjoint range) drains.  k_fused,
+// k_reduce and k_adam_gather wait for that launch before exiting, so stream
+// order still holds for whatever follows.
+cudaError_t launch_kernel(const void* fn, int grid, void** args, cudaStream_t s,
+                          bool overlap_prev);
 cudaError_t launch_fused(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s,
                          bool overlap_prev = false);
-cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s);
-cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
+cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s,
+                          bool overlap_prev = false);
+cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s,
+                               bool overlap_prev = false);
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
 // The literal ring schedule of zdp_step_ring (zdp_ring.cu); `ws` holds the

@@ -501,6 +501,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
 // Reduce-scatter only: reduced gradients to gout.
 template <int PT, bool EXACT, int GT, bool VEC>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ KParams p) {
+  allow_next_launch();
   const int P = ranks<PT, EXACT>(p);
   const bool sq = p.sumsq != nullptr;
   bool bad = false;
@@ -538,14 +539,17 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ KPa
     }
   }
   publish(p, bad, ss);
+  wait_previous_launch();
 }
 
 // AdamW from reduced gradients gin, then cast + all-gather into nrep
 // replicas.  With a gate, nothing is written when *gate != 0.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) k_adam_gather(const __grid_constant__ KParams p) {
+  allow_next_launch();
   if (p.gate && *p.gate) {  // uniform over the grid: the whole launch writes nothing
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.flag) atomicOr(p.flag, 1);
+    wait_previous_launch();
     return;
   }
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -593,6 +597,7 @@ __global__ void __launch_bounds__(kThreads) k_adam_gather(const __grid_constant_
       for (int q = 0; q < p.nrep; ++q) p.rep[q][i] = b;
     }
   }
+  wait_previous_launch();
 }
 
 // Cast + all-gather: rep[q][i] = bf16(w[i]).
