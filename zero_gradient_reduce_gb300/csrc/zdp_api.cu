@@ -1,6 +1,7 @@
 // zdp_api.cu -- the C ABI of libzdp: argument checks, kernel parameters and
 // launches.  Declarations and their documentation are in include/zdp.h.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -62,19 +63,24 @@ void add_range(std::vector<Range>& rs, const void* p, int64_t bytes, const char*
   if (p && bytes > 0) rs.push_back({addr(p), addr(p) + static_cast<uintptr_t>(bytes), what, idx});
 }
 
+// SM count of the current device, cached per device (any host thread may call).
 int num_sms(int* out) {
-  static int cache[128] = {0};
+  static std::atomic<int> cache[128];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev >= 0 && dev < 128 && cache[dev] > 0) {
-    *out = cache[dev];
-    return ZDP_OK;
+  const bool cached = dev >= 0 && dev < 128;
+  if (cached) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return ZDP_OK;
+    }
   }
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  if (dev >= 0 && dev < 128) cache[dev] = sms;
+  if (cached) cache[dev].store(sms, std::memory_order_relaxed);
   *out = sms;
   return ZDP_OK;
 }
