@@ -712,9 +712,11 @@ def run_reference(args):
 
 
 def run_sweep(args):
-    """GB/s of the overflow-checked step (two passes: reduced gradients to the
-    workspace, then the flag-gated AdamW + all-gather) against n and P, fp16
-    gradients scaled by 2^16.  Cold: the L2 is flushed (a write of twice its
+    """GB/s of the overflow-checked step against n and P, fp16 gradients scaled
+    by 2^16.  Ranges that fit one resident wave take the single-pass
+    cooperative form, larger ones two passes (reduced gradients to the
+    workspace, then the flag-gated AdamW + all-gather); the GB/s figure counts
+    the two-pass bytes either way.  Cold: the L2 is flushed (a write of twice its
     size) before every timed step; warm: steps back to back.  Bytes per step
     are (2P + 4) n for the first pass and (4 + 24 + 2P) n for the second."""
     import torch
@@ -772,7 +774,7 @@ def run_sweep(args):
             print(json.dumps({"sweep": "fp16_checked_step", "P": P, "n": n,
                               "us_cold": cold * 1e3, "us_warm": warm * 1e3,
                               "GBps_cold": nbytes / cold / 1e6, "GBps_warm": nbytes / warm / 1e6,
-                              "bytes_per_step": nbytes, "launches_per_step": 2,
+                              "bytes_per_step": nbytes,
                               "overflow_flag": int(words[0:4].view(torch.int32).item())}),
                   flush=True)
             del grads, st, reps_buf, ws, keep

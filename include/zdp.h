@@ -84,6 +84,11 @@ enum {
   ZDP_MAX_P = 64
 };
 
+/* Bits of the d_overflow word. */
+#define ZDP_FLAG_OVERFLOW 1 /* some reduced gradient was not finite */
+#define ZDP_FLAG_TIMEOUT 2  /* the single-pass checked step's grid barrier timed out: the
+                               blocks that gave up wrote nothing (see zdp_step) */
+
 /* Library version, e.g. 100 for 0.1.0. */
 int zdp_version(void);
 
@@ -151,8 +156,9 @@ typedef struct zdp_step_args {
                                  elements (one launch each); 0: whole range at once */
   int check_overflow;         /* nonzero: if any reduced gradient in the range is not
                                  finite, write nothing to master/m/v/replicas */
-  int32_t* d_overflow;        /* nullable device int32, OR-ed with 1 on a non-finite
-                                 reduced gradient in the range */
+  int32_t* d_overflow;        /* nullable device int32, OR-ed with ZDP_FLAG_OVERFLOW (1)
+                                 on a non-finite reduced gradient in the range, and
+                                 with ZDP_FLAG_TIMEOUT (2) as zdp_step describes */
   double* d_sumsq;            /* nullable device double; the fp64 sum of squares of
                                  the reduced gradients of the range is added */
   void* workspace;            /* device scratch for check_overflow (else unused), at
@@ -174,7 +180,17 @@ size_t zdp_step_workspace_bytes(const zdp_step_args* args);
  * With check_overflow the call makes two passes: the first stores the
  * reduced gradients in the workspace and raises a device flag on any
  * non-finite value; the second, skipped on the device when the flag is set,
- * applies AdamW and the all-gather.  The skip decision covers this call's
+ * applies AdamW and the all-gather.  When the 16-byte vector path applies, P
+ * is 1..8, 16, 32 or 64, and the range's reduced gradients fit in the
+ * registers of one resident wave (about 2 million elements on a GB300), it
+ * instead makes one cooperative launch that keeps them in registers across a
+ * grid barrier (same results, 8 fewer bytes per element and one launch
+ * instead of two).  That barrier waits at most ZDP_COOP_TIMEOUT_NS
+ * nanoseconds (environment variable, default 1e9); a block that gives up
+ * writes nothing and ORs ZDP_FLAG_TIMEOUT into *d_overflow.  Environment
+ * variable ZDP_COOP=0 selects the two-pass form always, and
+ * ZDP_TEST_COOP_EXTRA_ARRIVALS=k (tests only) makes the barrier wait for k
+ * arrivals that never come.  The skip decision covers this call's
  * range only; a caller streaming one step through several calls and wanting
  * a step-wide skip must check every range first (e.g. with
  * zdp_reduce_scatter into a scratch buffer).  A skipped step leaves t to the

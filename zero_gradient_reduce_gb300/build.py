@@ -27,7 +27,7 @@ NVCC_FLAGS = [
     f"-I{INCLUDE}", f"-I{CSRC}",
 ]
 UNITS = ["zdp_api.cu", "kernels_common.cu", "kernels_bf16.cu", "kernels_fp16.cu",
-         "zdp_noalloc.cu", "zdp_ring.cu", "zdp_zpp.cu", "zdp_copy.cu"]
+         "zdp_noalloc.cu", "zdp_ring.cu", "zdp_zpp.cu", "zdp_copy.cu", "zdp_coop.cu"]
 
 
 def nvcc() -> str:

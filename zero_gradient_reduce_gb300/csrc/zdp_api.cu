@@ -391,6 +391,17 @@ int zdp_step(const zdp_step_args* a, void* stream) {
     return ok();
   }
 
+  if (vec) {  // one cooperative launch when the range fits one resident wave
+    p.lo = off;
+    p.hi = off + len;
+    p.flag = a->d_overflow;
+    p.sumsq = a->d_sumsq;
+    bool launched = false;
+    cudaError_t e = zdp::launch_step_coop(p, a->gdt, sms, a->workspace, s, &launched);
+    if (e != cudaSuccess) return cuda_fail(e, "single-pass checked step launch");
+    if (launched) return ok();
+  }
+
   // Two passes: reduced gradients and a device flag, then the gated update.
   int32_t* ws_flag = static_cast<int32_t*>(a->workspace);
   float* ws_g = reinterpret_cast<float*>(static_cast<char*>(a->workspace) + 256);

@@ -113,6 +113,12 @@ cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cuda
                           bool overlap_prev = false);
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s,
                                bool overlap_prev = false);
+// The overflow-checked step in one cooperative launch over [p.lo, p.hi)
+// (16-byte vector path only).  ws: the call's workspace, whose first 8 bytes
+// it zeroes and uses.  Sets *launched = false, launching nothing, when the
+// range does not fit one resident wave, P has no template, or ZDP_COOP=0.
+cudaError_t launch_step_coop(const KParams& p, int gdt, int num_sms, void* ws, cudaStream_t s,
+                             bool* launched);
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s);
 
 // The literal ring schedule of zdp_step_ring (zdp_ring.cu); `ws` holds the
