@@ -483,7 +483,12 @@ def run_streamed(args, wl, dev, seed, rank, world):
                                d_sumsq=words[8:16].view(torch.float64), **HP)
             for lo, hi in bounds]
     step_ms = []
+    sampler = None
     for step in range(args.warmup + args.steps):
+        if step == args.warmup:
+            sampler = ClockSampler(gpu_id_for_smi(dev.index or 0))
+            sampler.start()
+            wall0 = time.time()
         words.zero_()
         ms = 0.0
         for (lo, hi), (a, _) in zip(bounds, argv):
@@ -498,6 +503,8 @@ def run_streamed(args, wl, dev, seed, rank, world):
             ms += e0.elapsed_time(e1)
         if step >= args.warmup:
             step_ms.append(ms)
+    wall1 = time.time()
+    sampler.stop()
     total_ms = max_over_ranks([sum(step_ms)], dev)[0]
     if rank != 0:
         return
@@ -516,6 +523,7 @@ def run_streamed(args, wl, dev, seed, rank, world):
                      "frac": alg_bytes / (total_ms / K / 1e3) / 1e9 / peak, "traffic": None,
                      "peak_source": f"{peak_kind} HBM copy bandwidth"},
         "gpu_launches": K * len(bounds),
+        "clocks": sampler.summary(wall0, wall1),
         "metric_note": f"measured on the {wl.name} workload, not the 1.3B headline",
     }), flush=True)
 

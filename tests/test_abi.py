@@ -188,3 +188,25 @@ def test_quantizer_rejects_bad_arguments(lib):
         zdp.zdp_quantize_blocks(FAKE, zdp.ZDP_F32, 1000, FAKE + 16, FAKE + 8192, stream=0)
     with pytest.raises(zdp.ZdpError, match="overlap"):
         zdp.zdp_dequantize_blocks(FAKE, FAKE + 8192, 1000, FAKE + 500, stream=0)
+
+
+def test_keepalive_holds_every_buffer_passed_in(lib):
+    # The struct stores raw addresses; the keepalive must keep the objects
+    # behind them alive, or a tensor made inline would be freed at once.
+    import gc
+    import weakref
+
+    import torch
+    grads = [torch.zeros(16, dtype=torch.bfloat16) for _ in range(2)]
+    reps = [torch.zeros(16, dtype=torch.bfloat16) for _ in range(2)]
+    state = [torch.zeros(16) for _ in range(3)]
+    refs = [weakref.ref(x) for x in (*grads, *reps, *state)]
+    a, keep = zdp.make_step_args(grads, *state, reps, n=16, scale=0.5, t=1, lr=1e-3, b1=0.9,
+                                 b2=0.95, eps=1e-8, wd=0.0)
+    del grads, reps, state
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    del keep
+    gc.collect()
+    assert all(r() is None for r in refs)
+

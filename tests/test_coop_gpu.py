@@ -5,8 +5,8 @@ zdp_step with check_overflow makes one cooperative launch with a grid barrier
 instead of two passes through the workspace.  The two forms must give the
 same bits: the state, the replicas and the flag word.  The sum of squares
 agrees to rounding, because its summation order follows the launch shape.
-They are compared here across P, sizes and injected
-infinities; the environment variable ZDP_COOP=0 forces the two-pass form.
+They are compared here across P, sizes, fp32 and bf16 moments and
+injected infinities; the environment variable ZDP_COOP=0 forces the two-pass form.
 The barrier's wait is bounded; a test makes it run out (it waits for an
 arrival that never comes) and checks that the flag word reports it, that
 nothing was written, and that the next call works.
@@ -22,10 +22,10 @@ from harness import DeviceStep, HP, assert_bits_equal, random_problem
 pytestmark = pytest.mark.gpu
 
 
-def _run(P, n, gbits, w, m, v, rep, bucket=0, coop=True, monkeypatch=None):
+def _run(P, n, gbits, w, m, v, rep, bucket=0, coop=True, monkeypatch=None, moments="f32"):
     if monkeypatch is not None:
         monkeypatch.setenv("ZDP_COOP", "1" if coop else "0")
-    dev = DeviceStep(P, n, torch.float16)
+    dev = DeviceStep(P, n, torch.float16, moments=moments)
     dev.load(gbits, w, m, v, rep)
     dev.step(1.0 / (P * 65536.0), 6, check_overflow=True, bucket_elems=bucket)
     torch.cuda.synchronize()
@@ -47,13 +47,16 @@ def _same(a, b, label):
 @pytest.mark.parametrize("P", [1, 3, 8, 16, 64])
 @pytest.mark.parametrize("n", [1, 9, 4097, 100_003, 1 << 20])
 @pytest.mark.parametrize("inject", [False, True])
-def test_single_pass_equals_two_pass(P, n, inject, monkeypatch):
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+def test_single_pass_equals_two_pass(P, n, inject, moments, monkeypatch):
     gbits, w, m, v = random_problem(P, n, P * 7 + n, oracle.FP16)
+    if moments == "bf16":
+        m, v = oracle.f32_to_bf16(m), oracle.f32_to_bf16(v)
     if inject:
         gbits[P - 1, n // 2] = 0x7C00  # +inf
     rep = np.full((P, n), 0x3F80, np.uint16)
-    a = _run(P, n, gbits, w, m, v, rep, coop=True, monkeypatch=monkeypatch)
-    b = _run(P, n, gbits, w, m, v, rep, coop=False, monkeypatch=monkeypatch)
+    a = _run(P, n, gbits, w, m, v, rep, coop=True, monkeypatch=monkeypatch, moments=moments)
+    b = _run(P, n, gbits, w, m, v, rep, coop=False, monkeypatch=monkeypatch, moments=moments)
     assert int(a.flag.item()) == (1 if inject else 0)
     _same(a, b, f"P={P} n={n} inject={inject}")
 

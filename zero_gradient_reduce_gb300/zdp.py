@@ -237,8 +237,10 @@ def make_step_args(grads: Sequence[Ptr], master: Ptr, m: Ptr, v: Ptr, replicas: 
 
     moments: "f32" (m and v fp32) or "bf16" (m and v bf16 buffers).
 
-    Returns (args, keepalive): the pointer arrays in `keepalive` back the
-    struct's grads/replicas fields and must outlive every use of `args`.
+    Returns (args, keepalive).  `keepalive` holds the pointer arrays behind
+    the struct's grads/replicas fields and every object passed in (so tensors
+    made inline, e.g. clones in the argument list, are not freed while their
+    addresses sit in `args`); it must outlive every use of `args`.
     """
     P = len(grads)
     len_ = (n - off) if length is None else length
@@ -265,7 +267,8 @@ def make_step_args(grads: Sequence[Ptr], master: Ptr, m: Ptr, v: Ptr, replicas: 
     a.workspace = _addr(workspace)
     a.workspace_bytes = workspace_bytes
     a.moment_dtype = {"f32": ZDP_MOMENTS_F32, "bf16": ZDP_MOMENTS_BF16}[moments]
-    return a, (garr, rarr)
+    return a, (garr, rarr, list(grads), list(replicas), master, m, v, d_overflow, d_sumsq,
+               workspace)
 
 
 def zdp_step_workspace_bytes(args: zdp_step_args) -> int:
@@ -311,7 +314,8 @@ def make_zpp_args(grads: Sequence[Ptr], grad_scales: Sequence[Ptr], master: Ptr,
                   lr: float, b1: float, b2: float, eps: float, wd: float, t: int, off: int = 0,
                   length: Optional[int] = None, d_overflow: Ptr = None, d_sumsq: Ptr = None,
                   moments: str = "f32"):
-    """Builds a zdp_zpp_args; returns (args, keepalive) as make_step_args."""
+    """Builds a zdp_zpp_args; returns (args, keepalive) as make_step_args
+    (keepalive also holds every object passed in)."""
     arrs = [_ptr_array(x) for x in (grads, grad_scales, replicas, replica_scales)]
     a = zdp_zpp_args()
     a.grads, a.grad_scales, a.replicas, a.replica_scales = [
@@ -323,7 +327,8 @@ def make_zpp_args(grads: Sequence[Ptr], grad_scales: Sequence[Ptr], master: Ptr,
     a.P = len(grads)
     a.scale, a.lr, a.b1, a.b2, a.eps, a.wd, a.t = scale, lr, b1, b2, eps, wd, t
     a.d_overflow, a.d_sumsq = _addr(d_overflow), _addr(d_sumsq)
-    return a, arrs
+    return a, (arrs, list(grads), list(grad_scales), list(replicas), list(replica_scales),
+               master, m, v, d_overflow, d_sumsq)
 
 
 def zdp_step_zpp(args: zdp_zpp_args, stream=None) -> None:
