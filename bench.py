@@ -78,6 +78,9 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="fp16 overflow-checked step over n = 1K..256M and P = 2..64: one "
                          "JSON line per point (cold and warm L2) instead of the benchmark line")
+    ap.add_argument("--unfused", action="store_true",
+                    help="the three-call chain zdp_reduce_scatter -> zdp_adamw_shard -> "
+                         "zdp_all_gather against the fused step, per-stage times: one JSON line")
     return ap.parse_args()
 
 
@@ -920,6 +923,96 @@ def run_zpp(args):
     }), flush=True)
 
 
+def run_unfused(args):
+    """The unfused chain of the step: zdp_reduce_scatter into an fp32 shard
+    buffer, zdp_adamw_shard on the whole padded range, zdp_all_gather of the
+    master into the replicas.  Each stage is timed with CUDA events on the
+    stream (median of `steps`), then the chain, then the fused zdp_step on
+    the same buffers.  Algorithmic bytes per parameter: (2P + 4) for the
+    reduce-scatter, 4 + 12 + 12 for AdamW, 4 + 2P for the all-gather:
+    4P + 36 in all, against 4P + 24 fused."""
+    import torch
+
+    from zero_gradient_reduce_gb300 import workloads, zdp
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    zdp.load()
+    wl = workloads.by_name(args.workload)
+    P, n = wl.P, wl.n
+    S = -(-n // P)
+    grads = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    for q in range(P):
+        workloads.fill_grads(grads[q], wl, q, 0, args.seed)
+    st = torch.empty(3, P * S, dtype=torch.float32, device=dev)
+    workloads.fill_state(st[0], st[1], st[2], wl, args.seed)
+    shards = torch.empty(P * S, dtype=torch.float32, device=dev)
+    reps = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    words = torch.zeros(16, dtype=torch.uint8, device=dev)
+    flag = words[0:4].view(torch.int32)
+    stream = torch.cuda.current_stream(dev)
+    a, keep = zdp.make_step_args(grads, st[0], st[1], st[2], reps, n=n, scale=wl.scale, t=1,
+                                 d_overflow=flag, **HP)
+    t = 0
+
+    def rs():
+        zdp.zdp_reduce_scatter(grads, shards, n, P, wl.scale, d_overflow=flag, stream=stream)
+
+    def adam():
+        zdp.zdp_adamw_shard(st[0], st[1], st[2], shards, P * S, t=t, stream=stream, **HP)
+
+    def ag():
+        zdp.zdp_all_gather(st[0], reps, n, P, stream=stream)
+
+    def chain():
+        rs()
+        adam()
+        ag()
+
+    def fused():
+        a.t = t
+        zdp.zdp_step(a, stream)
+
+    def timed(fn):
+        nonlocal t
+        ms = []
+        for k in range(args.warmup + args.steps):
+            t += 1
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if k >= args.warmup:
+                ms.append(e0.elapsed_time(e1))
+        return sorted(ms)[len(ms) // 2]
+
+    sampler = ClockSampler(gpu_id_for_smi(0))
+    sampler.start()
+    wall0 = time.time()
+    res = {name: timed(fn) for name, fn in
+           (("reduce_scatter", rs), ("adamw_shard", adam), ("all_gather", ag), ("chain", chain),
+            ("fused", fused))}
+    wall1 = time.time()
+    sampler.stop()
+    peak, peak_kind = measured_peak()
+    stage_bytes = {"reduce_scatter": (2 * P + 4) * n, "adamw_shard": 28 * P * S,
+                   "all_gather": (4 + 2 * P) * n, "chain": (4 * P + 36) * n,
+                   "fused": (4 * P + 24) * n}
+    stages = {k: {"ms": res[k], "alg_bytes": stage_bytes[k],
+                  "frac_of_copy": stage_bytes[k] / (res[k] / 1e3) / 1e9 / peak} for k in res}
+    print(json.dumps({
+        "metric": METRIC, "value": n / (res["chain"] / 1e3), "unit": "params/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["chain"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic, as the main benchmark", "config": dict(config_of(wl), path="unfused"),
+        "stages": stages, "fused_over_chain_speedup": res["chain"] / res["fused"],
+        "gpu_launches": 5 * args.steps, "clocks": sampler.summary(wall0, wall1),
+        "peak_source": f"{peak_kind} HBM copy bandwidth",
+        "metric_note": "the unfused three-call chain, not the headline",
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -930,6 +1023,8 @@ def main():
         run_sweep(args)
     elif args.ring_study:
         run_ring_study(args)
+    elif args.unfused:
+        run_unfused(args)
     else:
         run_ours(args)
 
