@@ -95,7 +95,7 @@ cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStre
 cudaError_t launch_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s) {
   const void* fn = vec ? reinterpret_cast<const void*>(&k_gather<true>)
                        : reinterpret_cast<const void*>(&k_gather<false>);
-  return launch_fn(fn, p, vec, num_sms, ZDP_CAP_GATHER, s);
+  return launch_fn(fn, p, vec, num_sms, gather_cap(p.nrep), s);
 }
 
 }  // namespace zdp

@@ -20,8 +20,8 @@ constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming ker
 // more threads are resident; the caps are the measured optima on GB300
 // (fused step: 512 threads per SM for P >= 4, 640 for P <= 3, where each
 // thread has fewer bytes in flight; reduce-scatter, which keeps only its
-// gradient loads in flight, 1536 and 1024; AdamW 640; AdamW with the replica
-// stores 512; all-gather 384).
+// gradient loads in flight: see reduce_cap; AdamW 640; AdamW with the replica
+// stores 512; all-gather: see gather_cap).
 #ifndef ZDP_CAP_FUSED
 #define ZDP_CAP_FUSED 4
 #endif
@@ -43,21 +43,24 @@ inline int fused_cap(int P, int mt) {
   if (P <= 3) return ZDP_CAP_FUSED_BF16M_SMALL_P;
   return P < 8 ? 8 : (P < 16 ? 7 : 6);
 }
-#ifndef ZDP_CAP_REDUCE
-#define ZDP_CAP_REDUCE 12
-#endif
-#ifndef ZDP_CAP_REDUCE_SMALL_P
-#define ZDP_CAP_REDUCE_SMALL_P 8
-#endif
+
+// Blocks per SM of the reduce-scatter for P ranks; measured fractions of the
+// copy ceiling at the chosen caps: P = 2: 8 blocks, 0.95; P = 4: 16, 0.99
+// (12: 0.96); P = 8, 16, 64: 12, 0.98-0.99.
+inline int reduce_cap(int P) { return P <= 3 ? 8 : (P < 8 ? 16 : 12); }
 #ifndef ZDP_CAP_ADAM
 #define ZDP_CAP_ADAM 5
 #endif
 #ifndef ZDP_CAP_ADAM_GATHER
 #define ZDP_CAP_ADAM_GATHER 4
 #endif
-#ifndef ZDP_CAP_GATHER
-#define ZDP_CAP_GATHER 3
-#endif
+
+// Blocks per SM of the all-gather for P replicas.  A thread reads 32 bytes
+// and writes 16P per vector, so small P needs more threads for the same
+// bytes in flight; measured fractions of the copy ceiling at the chosen caps:
+// P = 1 and 2: 8 blocks, 0.97 and 1.00 (3 blocks: 0.64 at P = 2); P = 4: 6,
+// 0.94; P = 8: 3, 0.93; P >= 16: 2, 0.88-0.89.
+inline int gather_cap(int P) { return P <= 2 ? 8 : (P <= 4 ? 6 : (P <= 8 ? 3 : 2)); }
 constexpr int kVec = 8;        // elements per vector: 16 B of bf16, 32 B of fp32
 
 // AdamW constants, prepared once per call on the host.
