@@ -18,16 +18,9 @@ constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming ker
 // kernel's registers do not allow it).  HBM throughput of these kernels
 // peaks at a moderate number of loads in flight per SM and falls again when
 // more threads are resident; the caps are the measured optima on GB300
-// (fused step: 512 threads per SM for P >= 4, 640 for P <= 3, where each
-// thread has fewer bytes in flight; reduce-scatter, which keeps only its
-// gradient loads in flight: see reduce_cap; AdamW 640; AdamW with the replica
-// stores 512; all-gather: see gather_cap).
-#ifndef ZDP_CAP_FUSED
-#define ZDP_CAP_FUSED 4
-#endif
-#ifndef ZDP_CAP_FUSED_SMALL_P
-#define ZDP_CAP_FUSED_SMALL_P 5
-#endif
+// (fused step: see fused_cap; reduce-scatter, which keeps only its gradient
+// loads in flight: see reduce_cap; AdamW 640 threads per SM; AdamW with the
+// replica stores 512; all-gather: see gather_cap).
 #ifndef ZDP_CAP_FUSED_BF16M_SMALL_P
 #define ZDP_CAP_FUSED_BF16M_SMALL_P 12
 #endif
@@ -35,11 +28,20 @@ constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming ker
 #define ZDP_CAP_ADAM_GATHER_BF16M 7
 #endif
 
-// Blocks per SM of the fused step for P ranks and the moment type, from the
-// measurements above (bf16 moments leave fewer bytes in flight per thread
-// and want more threads: 8 blocks at P = 4..7, 7 at P = 8..15, 6 above).
+// Blocks per SM of the fused step for P ranks and the moment type.  With
+// fp32 moments, measured over caps 2..8 for P = 1..16, 24, 32, 40, 48, 56, 64
+// (fraction of the copy ceiling at the chosen cap): P = 1: 5 (0.94); 2: 6
+// (0.95; 5 gave 0.87); 3: 5 (0.96); 4: 4 (0.95); 5..7: 5 (0.97-0.98); 8: 4
+// (0.97); 9..15, the partial-group template: 3 (0.95-0.99); 16..32: 4
+// (0.94-0.99); above 32: 3 (0.98-0.99 at 40, 48, 56, 64).  The optimum is
+// not monotonic in P: it follows each template's registers and bytes in
+// flight.  bf16 moments leave fewer bytes in flight per thread and want more
+// threads: 12 blocks at P <= 3, 8 at P = 4..7, 7 at P = 8..15, 6 above.
 inline int fused_cap(int P, int mt) {
-  if (mt == ZDP_MOMENTS_F32) return P <= 3 ? ZDP_CAP_FUSED_SMALL_P : ZDP_CAP_FUSED;
+  if (mt == ZDP_MOMENTS_F32) {
+    if (P <= 8) return P == 2 ? 6 : ((P == 4 || P == 8) ? 4 : 5);
+    return P < 16 ? 3 : (P <= 32 ? 4 : 3);
+  }
   if (P <= 3) return ZDP_CAP_FUSED_BF16M_SMALL_P;
   return P < 8 ? 8 : (P < 16 ? 7 : 6);
 }
