@@ -87,8 +87,7 @@ cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStre
                                bool overlap_prev) {
   const void* fn = vec ? reinterpret_cast<const void*>(&k_adam_gather<true>)
                        : reinterpret_cast<const void*>(&k_adam_gather<false>);
-  const int cap = p.nrep == 0 ? ZDP_CAP_ADAM
-                  : (p.mt == ZDP_MOMENTS_F32 ? ZDP_CAP_ADAM_GATHER : ZDP_CAP_ADAM_GATHER_BF16M);
+  const int cap = p.nrep == 0 ? ZDP_CAP_ADAM : adam_gather_cap(p.nrep, p.mt);
   return launch_fn(fn, p, vec, num_sms, cap, s, overlap_prev);
 }
 

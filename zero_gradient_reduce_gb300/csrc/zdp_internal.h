@@ -20,7 +20,7 @@ constexpr int kThreads = ZDP_THREADS;  // threads per block of the streaming ker
 // more threads are resident; the caps are the measured optima on GB300
 // (fused step: see fused_cap; reduce-scatter, which keeps only its gradient
 // loads in flight: see reduce_cap; AdamW 640 threads per SM; AdamW with the
-// replica stores 512; all-gather: see gather_cap).
+// replica stores: see adam_gather_cap; all-gather: see gather_cap).
 #ifndef ZDP_CAP_FUSED_BF16M_SMALL_P
 #define ZDP_CAP_FUSED_BF16M_SMALL_P 12
 #endif
@@ -53,9 +53,16 @@ inline int reduce_cap(int P) { return P <= 3 ? 8 : (P < 8 ? 16 : 12); }
 #ifndef ZDP_CAP_ADAM
 #define ZDP_CAP_ADAM 5
 #endif
-#ifndef ZDP_CAP_ADAM_GATHER
-#define ZDP_CAP_ADAM_GATHER 4
-#endif
+
+// Blocks per SM of the flag-gated AdamW + all-gather (the checked step's
+// second pass) for P replicas and the moment type; with fp32 moments,
+// measured on the two-pass checked step: P = 2: 5 (0.92 of the copy
+// ceiling; 4 gave 0.87); P = 4: 4 (0.98); P = 8 and 16: 3 (0.94, 0.93);
+// P = 64: any cap, 0.92.  bf16 moments: 7.
+inline int adam_gather_cap(int P, int mt) {
+  if (mt != ZDP_MOMENTS_F32) return ZDP_CAP_ADAM_GATHER_BF16M;
+  return P <= 2 ? 5 : (P <= 4 ? 4 : 3);
+}
 
 // Blocks per SM of the all-gather for P replicas.  A thread reads 32 bytes
 // and writes 16P per vector, so small P needs more threads for the same
