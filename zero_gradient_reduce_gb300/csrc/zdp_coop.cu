@@ -199,8 +199,11 @@ cudaError_t launch_step_coop(const KParams& p, int gdt, int num_sms, void* ws, c
   c.ws_flag = static_cast<int32_t*>(ws);
   c.arrived = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + 4);
   // A test hook: extra arrivals that never come make the barrier time out.
-  c.expected = static_cast<uint32_t>(grid + env_int("ZDP_TEST_COOP_EXTRA_ARRIVALS", 0));
-  c.timeout_ns = static_cast<uint64_t>(env_int("ZDP_COOP_TIMEOUT_NS", 1000000000));
+  // (never fewer than grid: the barrier must not open before every block arrived)
+  const int64_t extra = std::max<int64_t>(0, env_int("ZDP_TEST_COOP_EXTRA_ARRIVALS", 0));
+  c.expected = static_cast<uint32_t>(grid + std::min<int64_t>(extra, 1 << 20));
+  c.timeout_ns = static_cast<uint64_t>(
+      std::max<int64_t>(1000, env_int("ZDP_COOP_TIMEOUT_NS", 1000000000)));
   cudaError_t e = cudaMemsetAsync(ws, 0, 8, s);
   if (e != cudaSuccess) return e;
   void* args[] = {&c};
