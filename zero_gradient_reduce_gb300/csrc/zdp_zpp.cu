@@ -115,7 +115,9 @@ template <int PT>
 __device__ __forceinline__ void zpp_ring_vec(const ZppParams& p, int P, int r, int64_t i0,
                                              int64_t blk, float (&acc)[kVec]) {
   int q = ring_next(r, P);
-  constexpr int U = PT > 0 && PT < 8 ? PT : 8;
+  // The generic kernel (PT = 0) loads 4 ranks at a time: with 8 its predicated
+  // loads spilled 644 bytes and it ran 0.08 of the copy ceiling slower (P = 10..20).
+  constexpr int U = PT > 0 && PT < 8 ? PT : (PT == 0 ? 4 : 8);
   constexpr bool EXACT = PT > 0;
 #pragma unroll 1
   for (int base = 0; base < P; base += U) {
