@@ -27,7 +27,8 @@ NVCC_FLAGS = [
     f"-I{INCLUDE}", f"-I{CSRC}",
 ]
 UNITS = ["zdp_api.cu", "kernels_common.cu", "kernels_bf16.cu", "kernels_fp16.cu",
-         "zdp_noalloc.cu", "zdp_ring.cu", "zdp_zpp.cu", "zdp_copy.cu", "zdp_coop.cu"]
+         "zdp_noalloc.cu", "zdp_ring.cu", "zdp_zpp.cu", "zdp_copy.cu", "zdp_coop_bf16.cu",
+         "zdp_coop_fp16.cu"]
 
 
 def nvcc() -> str:

@@ -13,6 +13,10 @@ cudaError_t launch_fused_fp16(const KParams& p, bool vec, int num_sms, cudaStrea
                               bool overlap_prev);
 cudaError_t launch_reduce_bf16(const KParams& p, bool vec, int num_sms, cudaStream_t s,
                                bool overlap_prev);
+cudaError_t launch_step_coop_bf16(const KParams& p, int num_sms, void* ws, cudaStream_t s,
+                                  bool* launched);
+cudaError_t launch_step_coop_fp16(const KParams& p, int num_sms, void* ws, cudaStream_t s,
+                                  bool* launched);
 cudaError_t launch_reduce_fp16(const KParams& p, bool vec, int num_sms, cudaStream_t s,
                                bool overlap_prev);
 
@@ -75,6 +79,12 @@ cudaError_t launch_fused(const KParams& p, int gdt, bool vec, int num_sms, cudaS
                          bool overlap_prev) {
   return gdt == ZDP_BF16 ? launch_fused_bf16(p, vec, num_sms, s, overlap_prev)
                          : launch_fused_fp16(p, vec, num_sms, s, overlap_prev);
+}
+
+cudaError_t launch_step_coop(const KParams& p, int gdt, int num_sms, void* ws, cudaStream_t s,
+                             bool* launched) {
+  return gdt == ZDP_BF16 ? launch_step_coop_bf16(p, num_sms, ws, s, launched)
+                         : launch_step_coop_fp16(p, num_sms, ws, s, launched);
 }
 
 cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cudaStream_t s,
