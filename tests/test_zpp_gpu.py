@@ -147,6 +147,33 @@ def test_zpp_step_matches_the_oracle(P, moments):
         assert abs(float(words[8:16].view(torch.float64).item()) - ss) <= 1e-9 * ss
 
 
+@pytest.mark.parametrize("t", [200, 1000])
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+def test_zpp_step_in_steady_state_matches_the_oracle(t, moments):
+    # From t of a few hundred on, fl(1 - b^t) is exactly 1 (at t = 1000 for
+    # both betas, at t = 200 only for b1): the kernel's shortcut for that case
+    # must give the oracle's bits.
+    P, n = 8, 40_000
+    gq, gs, w, m, v = _zpp_problem(P, n, t + 1, moments)
+    dg, ds, dw, dm, dv, rq, rs = _to_dev(gq, gs, w, m, v, P, n, moments)
+    a, keep = zdp.make_zpp_args(dg, ds, dw, dm, dv, rq, rs, n=n, scale=1.0 / P, t=t,
+                                moments=moments, **HP)
+    zdp.zdp_step_zpp(a)
+    torch.cuda.synchronize()
+    nb = gs.shape[1]
+    wq, wsc = np.zeros((P, n), np.int8), np.zeros((P, nb), np.float32)
+    ww, mm, vv = w.copy(), m.copy(), v.copy()
+    oracle.step_zpp(gq, gs, ww, mm, vv, wq, wsc, n, 0, n, 1.0 / P, t=t, moments=moments, **HP)
+    assert_bits_equal(dw.cpu().numpy()[:n], ww[:n], f"t={t} master")
+    if moments == "f32":
+        assert_bits_equal(dm.cpu().numpy()[:n], mm[:n], f"t={t} m")
+        assert_bits_equal(dv.cpu().numpy()[:n], vv[:n], f"t={t} v")
+    else:
+        assert np.array_equal(bits_of(dm)[:n], mm[:n]) and np.array_equal(bits_of(dv)[:n], vv[:n])
+    for q in range(P):
+        assert np.array_equal(_i8(rq[q]), wq[q]), f"t={t} replica {q}"
+
+
 def test_zpp_sub_ranges_compose_to_the_whole():
     P, n = 4, 256 * 200 + 99
     gq, gs, w, m, v = _zpp_problem(P, n, 5)
