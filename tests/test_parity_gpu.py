@@ -68,6 +68,15 @@ def test_tiny_flat_config_full_parity():
     _compare_step(dev, w, m, v, rep, flag, ss, "tiny")
 
 
+@pytest.mark.parametrize("t", [200, 1000, 1_000_000])
+@pytest.mark.parametrize("gdt", [oracle.BF16, oracle.FP16])
+def test_fused_step_in_steady_state(t, gdt):
+    # From t of a few hundred on, fl(1 - b^t) rounds to exactly 1 (b1 first).
+    P, n = 8, 50_003
+    dev, (w, m, v, rep, flag, ss) = _full_case(P, n, seed=t % 997, gdt=gdt, t=t)
+    _compare_step(dev, w, m, v, rep, flag, ss, f"t={t}")
+
+
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16, 17, 64])
 def test_fused_step_edge_sizes(P):
     ns = sorted({1, 7, max(P - 1, 1), P, P + 1, 8 * P + 3, 1001, 3 * 8192 + 5})
