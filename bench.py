@@ -78,6 +78,10 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="fp16 overflow-checked step over n = 1K..256M and P = 2..64: one "
                          "JSON line per point (cold and warm L2) instead of the benchmark line")
+    ap.add_argument("--check-overflow", action="store_true",
+                    help="time the overflow-checked step (skip on a non-finite reduced "
+                         "gradient): one cooperative launch when the range fits one resident "
+                         "wave, else two passes through a workspace")
     ap.add_argument("--unfused", action="store_true",
                     help="the three-call chain zdp_reduce_scatter -> zdp_adamw_shard -> "
                          "zdp_all_gather against the fused step, per-stage times: one JSON line")
@@ -325,7 +329,11 @@ def run_ours(args):
 
     a, keep = zdp.make_step_args(grads, master, m, v, replicas, n=n, scale=wl.scale, t=1,
                                  bucket_elems=wl.bucket_elems, d_overflow=flag, d_sumsq=sumsq,
-                                 moments=args.moments, **HP)
+                                 moments=args.moments, check_overflow=args.check_overflow, **HP)
+    ws = None
+    if args.check_overflow:
+        ws = torch.empty(zdp.zdp_step_workspace_bytes(a), dtype=torch.uint8, device=dev)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
     # one fused launch per bucket (the whole range when the workload has no buckets)
     launches_per_step = -(-n // wl.bucket_elems) if wl.bucket_elems else 1
     stream = torch.cuda.current_stream(dev)
@@ -388,7 +396,7 @@ def run_ours(args):
 
     # ---- end to end through the C ABI: gradients from pinned host memory
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.check_overflow:
         e2e = run_e2e(args, wl, grads, master, m, v, replicas, words, flag, sumsq, dev, t)
         e2e["moments"] = args.moments
         slowest = max_over_ranks([e2e.get("seconds_per_step") or 0.0], dev)[0]
@@ -404,7 +412,8 @@ def run_ours(args):
         peak, peak_kind = measured_peak()
         alg_bytes = bytes_per_param(P, args.moments) * n
         achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
-        traffic = recorded_traffic(wl.name) if args.moments == "f32" else None
+        traffic = (recorded_traffic(wl.name)
+                   if args.moments == "f32" and not args.check_overflow else None)
         clocks = sampler.summary(wall0, wall1)
         out = {
             "metric": METRIC,
@@ -421,7 +430,7 @@ def run_ours(args):
             "data": "synthetic: seeded N(0, sigma_T) bf16 gradients (sigma_T log-uniform "
                     "[1e-5, 1e-2] per tensor), master ~ N(0, 0.02), m = v = 0 at t = 1",
             "config": dict(config_of(wl, wl.bucket_elems, flush is not None),
-                           moments=args.moments),
+                           moments=args.moments, check_overflow=bool(args.check_overflow)),
             "hbm_tbs": alg_bytes / (ms_per_step / 1e3) / 1e12,
             "roofline": {
                 "bound": "hbm",
@@ -431,7 +440,8 @@ def run_ours(args):
                 "frac": achieved / peak,
                 "traffic": traffic,
                 "peak_source": f"{peak_kind} HBM copy bandwidth",
-                "kernel": f"k_fused<P={P}, bf16>",
+                "kernel": (f"k_fused<P={P}, bf16>" if not args.check_overflow else
+                           "k_step_coop (one launch) or k_reduce + k_adam_gather (two passes)"),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "kernel_ms": kernel_ms,
                 "kernel_ms_median": kernel_ms_median,
@@ -442,16 +452,20 @@ def run_ours(args):
                 "zdp_copy_this_run_median": copies["zdp_copy"][1],
                 "frac_of_nominal_hbm": achieved / NOMINAL_HBM_GBS,
             },
-            "gpu_launches": K * launches_per_step,
+            "gpu_launches": K * launches_per_step * (2 if args.check_overflow else 1),
             "clocks": clocks,
             "overflow_flag": step_flag,
         }
         if e2e is not None:
             out["e2e"] = e2e
-        if world == 1 and not args.no_cpu_baseline:
+        if args.check_overflow:
+            out["metric_note"] = ("the overflow-checked step; the two-pass form moves 8 more "
+                                  "bytes per parameter than the algorithmic bytes above")
+        if world == 1 and not args.no_cpu_baseline and not args.check_overflow:
             out["cpu_baseline"] = cpu_baseline(args, wl, grads, master, m, v, P, n)
         if wl.name != workloads.gpt_1p3b().name:
-            out["metric_note"] = f"measured on the {wl.name} workload, not the 1.3B headline"
+            note = f"measured on the {wl.name} workload, not the 1.3B headline"
+            out["metric_note"] = note + ("; " + out["metric_note"] if "metric_note" in out else "")
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
