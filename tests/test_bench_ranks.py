@@ -82,3 +82,16 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["unit"] == "params/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_headline_profile_matches_the_kernel_sources():
+    # bench.py reports the committed ncu traffic only while the kernel sources
+    # hash to the value recorded beside it; a kernel change without a new
+    # capture would silently turn `traffic` into null.
+    sys.path.insert(0, ROOT)
+    import bench
+
+    traffic = bench.recorded_traffic("gpt_1.3B_p8")
+    assert traffic is not None, "kernel sources changed since profiles/ was captured"
+    alg = 56 * 1_311_227_904
+    assert 0.99 * alg < traffic < 1.01 * alg
