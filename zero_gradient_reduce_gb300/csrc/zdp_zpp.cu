@@ -359,8 +359,11 @@ cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cuda
     default: fn = reinterpret_cast<const void*>(&k_zpp<0>); break;
   }
   void* args[] = {&p};
-  return cudaLaunchKernel(fn, dim3(grid_warps(fn, blocks, num_sms, ZDP_CAP_ZPP)), dim3(kThreads),
-                          args, 0, s);
+  // 6 blocks per SM at P = 2 (0.90 of the copy ceiling against 0.88 with 8);
+  // every other P measured best at the register-limited 8 (or 6 above P = 8).
+  const int cap = P == 2 ? 6 : ZDP_CAP_ZPP;
+  return cudaLaunchKernel(fn, dim3(grid_warps(fn, blocks, num_sms, cap)), dim3(kThreads), args,
+                          0, s);
 }
 
 cudaError_t launch_quantize(const void* x, int xdt, int64_t n, int8_t* q, float* scales,
