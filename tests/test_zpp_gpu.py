@@ -147,6 +147,43 @@ def test_zpp_step_matches_the_oracle(P, moments):
         assert abs(float(words[8:16].view(torch.float64).item()) - ss) <= 1e-9 * ss
 
 
+@pytest.mark.parametrize("P", [2, 8, 16])
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+@pytest.mark.parametrize("exps", [(-90, -60), (40, 70), (-90, 70)])
+def test_zpp_sum_of_squares_at_extreme_scales(P, moments, exps):
+    # Block scales multiplied by powers of two 2^e, e drawn from `exps`, so
+    # that the squares of the reduced gradients fall below fp32's smallest
+    # subnormal, above its largest value, or both within each thread's
+    # share.  The P and moment types cover both accumulators of the kernel
+    # (fp64 at P = 2 and at P = 8 with bf16 moments, compensated fp32 at
+    # P = 8 with fp32 moments and at P = 16).
+    n = 256 * 16 * P + 77
+    gq, gs, w, m, v = _zpp_problem(P, n, 31 * P, moments)
+    rng = np.random.default_rng(P)
+    e = rng.integers(exps[0], exps[1] + 1, gs.shape)
+    gs = (gs * np.exp2(e).astype(np.float32)).astype(np.float32)
+    dg, ds, dw, dm, dv, rq, rs = _to_dev(gq, gs, w, m, v, P, n, moments)
+    words = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    a, keep = zdp.make_zpp_args(dg, ds, dw, dm, dv, rq, rs, n=n, scale=1.0 / P, t=3,
+                                d_overflow=words[0:4].view(torch.int32),
+                                d_sumsq=words[8:16].view(torch.float64), moments=moments, **HP)
+    zdp.zdp_step_zpp(a)
+    torch.cuda.synchronize()
+    nb = gs.shape[1]
+    wq, wsc = np.zeros((P, n), np.int8), np.zeros((P, nb), np.float32)
+    ww, mm, vv = w.copy(), m.copy(), v.copy()
+    flag, ss = oracle.step_zpp(gq, gs, ww, mm, vv, wq, wsc, n, 0, n, 1.0 / P, t=3,
+                               moments=moments, **HP)
+    label = f"extreme scales P={P} {moments} 2^{exps}"
+    assert flag == 0 and int(words[0:4].view(torch.int32).item()) == 0, label
+    assert 0.0 < ss < np.inf and (ss < 1e-30 if exps[1] < 0 else ss > 1e20), (label, ss)
+    got = float(words[8:16].view(torch.float64).item())
+    assert abs(got - ss) <= 1e-9 * ss, (label, got, ss)
+    assert_state_close(dw.cpu().numpy()[:n], ww[:n], label + " master")
+    for q in (0, P - 1):
+        assert np.array_equal(_i8(rq[q]), wq[q]), label + f" replica {q}"
+
+
 @pytest.mark.parametrize("t", [200, 1000])
 @pytest.mark.parametrize("moments", ["f32", "bf16"])
 def test_zpp_step_in_steady_state_matches_the_oracle(t, moments):

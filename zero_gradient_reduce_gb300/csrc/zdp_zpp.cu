@@ -10,6 +10,7 @@
 // reduction; the loops over blocks are warp-uniform.
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "zdp_kernels.cuh"
 
@@ -162,7 +163,44 @@ __device__ __forceinline__ void zpp_ring_vec(const ZppParams& p, int P, int r, i
 #define ZDP_ZPP_MIN_BLOCKS_WIDE 6
 #endif
 
-template <int PT>
+// The sum of squares accumulated straight in fp64: the square of an fp32
+// value has at most 48 significant bits and an exponent within fp64's range,
+// so it is exact in fp64 and each step rounds once (no worse than the
+// compensated fp32 SumSq).  It costs one fp64 fma per element where SumSq
+// spends about ten fp32 instructions.  GB300's fp64 rate is low, so which
+// form is faster depends on what else the kernel keeps busy; see
+// zpp_f64_sumsq.
+struct SumSqF64 {
+  double total = 0.0;
+  __device__ __forceinline__ void add(float g) {
+    const double d = static_cast<double>(g);
+    total = __fma_rn(d, d, total);
+  }
+};
+
+__device__ __forceinline__ void account(const float (&g)[kVec], bool sq, bool& bad,
+                                        SumSqF64& ss) {
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) bad |= non_finite(g[k]);
+  if (sq) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) ss.add(g[k]);
+  }
+}
+
+__device__ __forceinline__ void account1(float g, bool sq, bool& bad, SumSqF64& ss) {
+  bad |= non_finite(g);
+  if (sq) ss.add(g);
+}
+
+__device__ __forceinline__ void publish_to(int32_t* flag, double* sumsq, bool bad,
+                                           SumSqF64& acc) {
+  SumSq whole;  // carries the fp64 total through the block reduction
+  whole.total = acc.total;
+  publish_to(flag, sumsq, bad, whole);
+}
+
+template <int PT, bool F64SQ>
 __global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : ZDP_ZPP_MIN_BLOCKS)
     k_zpp(const __grid_constant__ ZppParams p) {
   const int P = PT > 0 ? PT : p.P;
@@ -171,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : Z
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
   bool bad = false;
-  SumSq ss;
+  typename std::conditional<F64SQ, SumSqF64, SumSq>::type ss;
   const int64_t b0 = p.lo / kQB, b1 = (p.hi + kQB - 1) / kQB;  // p.lo is block aligned
   for (int64_t b = b0 + warp; b < b1; b += nwarps) {               // warp-uniform
     const int64_t i0 = b * kQB + lane * kVec;
@@ -314,6 +352,32 @@ int grid_warps(const void* kernel, int64_t warps_needed, int num_sms, int cap) {
   return static_cast<int>(std::max<int64_t>(1, std::min(blocks, full)));
 }
 
+template <int PT>
+const void* zpp_kernel(bool f64) {
+  return f64 ? reinterpret_cast<const void*>(&k_zpp<PT, true>)
+             : reinterpret_cast<const void*>(&k_zpp<PT, false>);
+}
+
+// Whether the step with the sum of squares accumulates it in fp64
+// (SumSqF64) rather than compensated fp32 (SumSq), for P ranks and the
+// moment type: the faster form measured on GB300 with the sum of squares
+// asked for (time of the compensated form / time of the fp64 form, fp32
+// moments and bf16 moments): P = 2: 1.02, 1.06; 4: 1.07, 1.08; 5: 1.06,
+// 1.10; 8: 0.98, 1.12; 12 (the generic kernel): 1.09, 1.05; 16: 0.98, 0.96
+// (the wide template spills 76 bytes with the fp64 form; P = 32 shares
+// it); 64: 1.03, 0.99.  ZDP_ZPP_F64SQ = 0 or 1 forces one form (for tuning).
+#ifndef ZDP_ZPP_F64SQ
+#define ZDP_ZPP_F64SQ -1
+#endif
+bool zpp_f64_sumsq(int P, int mt) {
+  if (ZDP_ZPP_F64SQ >= 0) return ZDP_ZPP_F64SQ != 0;
+  const bool f32 = mt == ZDP_MOMENTS_F32;
+  if (P == 16 || P == 32) return false;
+  if (P == 8) return !f32;
+  if (P == 64) return f32;
+  return true;
+}
+
 }  // namespace
 
 cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cudaStream_t s) {
@@ -343,20 +407,21 @@ cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cuda
   p.sumsq = a->d_sumsq;
   const int64_t blocks = (a->len + kQB - 1) / kQB;
   if (blocks == 0) return cudaSuccess;
+  const bool f64 = p.sumsq != nullptr && zpp_f64_sumsq(P, p.mt);
   const void* fn;
   switch (P) {
-    case 1: fn = reinterpret_cast<const void*>(&k_zpp<1>); break;
-    case 2: fn = reinterpret_cast<const void*>(&k_zpp<2>); break;
-    case 3: fn = reinterpret_cast<const void*>(&k_zpp<3>); break;
-    case 4: fn = reinterpret_cast<const void*>(&k_zpp<4>); break;
-    case 5: fn = reinterpret_cast<const void*>(&k_zpp<5>); break;
-    case 6: fn = reinterpret_cast<const void*>(&k_zpp<6>); break;
-    case 7: fn = reinterpret_cast<const void*>(&k_zpp<7>); break;
-    case 8: fn = reinterpret_cast<const void*>(&k_zpp<8>); break;
-    case 16: fn = reinterpret_cast<const void*>(&k_zpp<16>); break;
-    case 32: fn = reinterpret_cast<const void*>(&k_zpp<32>); break;
-    case 64: fn = reinterpret_cast<const void*>(&k_zpp<64>); break;
-    default: fn = reinterpret_cast<const void*>(&k_zpp<0>); break;
+    case 1: fn = zpp_kernel<1>(f64); break;
+    case 2: fn = zpp_kernel<2>(f64); break;
+    case 3: fn = zpp_kernel<3>(f64); break;
+    case 4: fn = zpp_kernel<4>(f64); break;
+    case 5: fn = zpp_kernel<5>(f64); break;
+    case 6: fn = zpp_kernel<6>(f64); break;
+    case 7: fn = zpp_kernel<7>(f64); break;
+    case 8: fn = zpp_kernel<8>(f64); break;
+    case 16: fn = zpp_kernel<16>(f64); break;
+    case 32: fn = zpp_kernel<32>(f64); break;
+    case 64: fn = zpp_kernel<64>(f64); break;
+    default: fn = zpp_kernel<0>(f64); break;
   }
   void* args[] = {&p};
   // 6 blocks per SM at P = 2 (0.90 of the copy ceiling against 0.88 with 8);
