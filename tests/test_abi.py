@@ -210,3 +210,28 @@ def test_keepalive_holds_every_buffer_passed_in(lib):
     gc.collect()
     assert all(r() is None for r in refs)
 
+
+
+def test_binding_rejects_pointer_lists_of_the_wrong_length(lib):
+    # The library reads P pointers from each host array; a short list would
+    # be read past its end, so the binding refuses it before the call.
+    hp = dict(scale=0.5, t=1, lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.0)
+    g2, r1 = [FAKE, FAKE + 4096], [FAKE + 8192]
+    with pytest.raises(ValueError, match="different lengths"):
+        zdp.make_step_args(g2, FAKE + 16384, FAKE + 20480, FAKE + 24576, r1, n=16, **hp)
+    with pytest.raises(ValueError, match="outside"):
+        zdp.make_step_args([], FAKE + 16384, FAKE + 20480, FAKE + 24576, [], n=16, **hp)
+    with pytest.raises(ValueError, match="different lengths"):
+        zdp.make_zpp_args(g2, g2, FAKE + 16384, FAKE + 20480, FAKE + 24576, g2, r1, n=256, **hp)
+    with pytest.raises(ValueError, match="for P=3"):
+        zdp.zdp_reduce_scatter(g2, FAKE + 8192, 16, 3, 0.5, stream=0)
+    with pytest.raises(ValueError, match="for P=2"):
+        zdp.zdp_all_gather(FAKE, r1, 16, 2, stream=0)
+
+
+def test_binding_rejects_gradients_of_another_dtype(lib):
+    import torch
+    g = [torch.zeros(16, dtype=torch.float32) for _ in range(2)]
+    with pytest.raises(ValueError, match="bfloat16 or float16"):
+        zdp.make_step_args(g, FAKE + 16384, FAKE + 20480, FAKE + 24576, [FAKE, FAKE + 4096],
+                           n=16, scale=0.5, t=1, lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.0)

@@ -133,7 +133,6 @@ int zdp_reduce_scatter(const void* const* grads, int gdt, float* shards, int64_t
   if (!shards) return fail(ZDP_ERR_INVALID, "shards is NULL");
   if ((addr(shards) & 3u) != 0) return fail(ZDP_ERR_INVALID, "shards not 4-byte aligned");
   const int64_t S = shard(n, P);
-  std::vector<Range> rs;
   bool vec = aligned16(shards);
   for (int q = 0; q < P; ++q) {
     if (!grads[q]) return fail(ZDP_ERR_INVALID, "grads[%d] is NULL", q);

@@ -185,15 +185,34 @@ def _check(status: int):
 
 
 def _gdt(x, gdt):
+    """The gradient type: `gdt` when given, else from a tensor's dtype (bf16
+    or fp16; any other dtype is an error), else bf16 for raw addresses."""
     if gdt is not None:
         return gdt
     try:
         import torch
         if isinstance(x, torch.Tensor):
-            return ZDP_FP16 if x.dtype == torch.float16 else ZDP_BF16
+            if x.dtype == torch.float16:
+                return ZDP_FP16
+            if x.dtype == torch.bfloat16:
+                return ZDP_BF16
+            raise ValueError(f"gradients must be bfloat16 or float16, not {x.dtype}")
     except ImportError:  # pragma: no cover
         pass
     return ZDP_BF16
+
+
+def _same_lengths(**seqs):
+    """The library reads P pointers from each array: every list must hold
+    exactly P of them."""
+    lens = {k: len(v) for k, v in seqs.items()}
+    if len(set(lens.values())) != 1:
+        raise ValueError("pointer lists of different lengths: " +
+                         ", ".join(f"{k}={n}" for k, n in lens.items()))
+    P = next(iter(lens.values()))
+    if not 1 <= P <= ZDP_MAX_P:
+        raise ValueError(f"{P} ranks, outside 1..{ZDP_MAX_P}")
+    return P
 
 
 def zdp_version() -> int:
@@ -211,8 +230,11 @@ def zdp_last_error() -> str:
 def zdp_reduce_scatter(grads: Sequence[Ptr], shards: Ptr, n: int, P: int, scale: float,
                        d_overflow: Ptr = None, d_sumsq: Ptr = None, gdt: Optional[int] = None,
                        stream=None) -> None:
+    if len(grads) != P:
+        raise ValueError(f"{len(grads)} gradient pointers for P={P}")
     arr = _ptr_array(grads)
-    _check(load().zdp_reduce_scatter(arr, _gdt(grads[0] if grads else None, gdt), _addr(shards), n, P, scale,
+    _check(load().zdp_reduce_scatter(arr, _gdt(grads[0] if grads else None, gdt), _addr(shards),
+                                     n, P, scale,
                                      _addr(d_overflow), _addr(d_sumsq), _stream(stream)))
 
 
@@ -223,6 +245,8 @@ def zdp_adamw_shard(master: Ptr, m: Ptr, v: Ptr, grad_shard: Ptr, count: int, lr
 
 
 def zdp_all_gather(master: Ptr, replicas: Sequence[Ptr], n: int, P: int, stream=None) -> None:
+    if len(replicas) != P:
+        raise ValueError(f"{len(replicas)} replica pointers for P={P}")
     arr = _ptr_array(replicas)
     _check(load().zdp_all_gather(_addr(master), arr, n, P, _stream(stream)))
 
@@ -242,7 +266,7 @@ def make_step_args(grads: Sequence[Ptr], master: Ptr, m: Ptr, v: Ptr, replicas: 
     made inline, e.g. clones in the argument list, are not freed while their
     addresses sit in `args`); it must outlive every use of `args`.
     """
-    P = len(grads)
+    P = _same_lengths(grads=grads, replicas=replicas)
     len_ = (n - off) if length is None else length
     garr = _ptr_array(grads)
     rarr = _ptr_array(replicas)
@@ -316,6 +340,8 @@ def make_zpp_args(grads: Sequence[Ptr], grad_scales: Sequence[Ptr], master: Ptr,
                   moments: str = "f32"):
     """Builds a zdp_zpp_args; returns (args, keepalive) as make_step_args
     (keepalive also holds every object passed in)."""
+    P = _same_lengths(grads=grads, grad_scales=grad_scales, replicas=replicas,
+                      replica_scales=replica_scales)
     arrs = [_ptr_array(x) for x in (grads, grad_scales, replicas, replica_scales)]
     a = zdp_zpp_args()
     a.grads, a.grad_scales, a.replicas, a.replica_scales = [
@@ -324,7 +350,7 @@ def make_zpp_args(grads: Sequence[Ptr], grad_scales: Sequence[Ptr], master: Ptr,
     a.moment_dtype = {"f32": ZDP_MOMENTS_F32, "bf16": ZDP_MOMENTS_BF16}[moments]
     a.n, a.off = n, off
     a.len = (n - off) if length is None else length
-    a.P = len(grads)
+    a.P = P
     a.scale, a.lr, a.b1, a.b2, a.eps, a.wd, a.t = scale, lr, b1, b2, eps, wd, t
     a.d_overflow, a.d_sumsq = _addr(d_overflow), _addr(d_sumsq)
     return a, (arrs, list(grads), list(grad_scales), list(replicas), list(replica_scales),
