@@ -743,7 +743,15 @@ def run_sweep(args):
     workspace, then the flag-gated AdamW + all-gather); the GB/s figure counts
     the two-pass bytes either way.  Cold: the L2 is flushed (a write of twice its
     size) before every timed step; warm: steps back to back.  Bytes per step
-    are (2P + 4) n for the first pass and (4 + 24 + 2P) n for the second."""
+    are (2P + 4) n for the first pass and (4 + 24 + 2P) n for the second.
+
+    A seeded 1 % of the runs (warm-up included) get one +inf, -inf or NaN at a
+    seeded (rank, index) of the fp16 gradients, written before the run's
+    start event and undone after its end event.  The flag word is cleared
+    before every run; each run's flag must be 1 exactly when it was injected,
+    and an injected (skipped) step does not advance t.  Each line reports the
+    injected runs and whether every flag matched."""
+    import numpy as np
     import torch
 
     from zero_gradient_reduce_gb300 import workloads, zdp
@@ -771,17 +779,36 @@ def run_sweep(args):
                                          d_overflow=words[0:4].view(torch.int32), **HP)
             ws = torch.empty(zdp.zdp_step_workspace_bytes(a), dtype=torch.uint8, device=dev)
             a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+            runs = args.warmup + 2 * reps
+            rng = np.random.default_rng([args.seed, P, n])
+            inject = rng.random(runs) < 0.01
+            where = [(int(rng.integers(P)), int(rng.integers(n)),
+                      int(rng.choice([0x7C00, 0xFC00, 0x7E00]))) for _ in range(runs)]
+            flag = words[0:4].view(torch.int32)
+            flags = torch.zeros(runs, dtype=torch.int32, device=dev)
             t = 0
+            run = 0
 
             def one(e0=None, e1=None):
-                nonlocal t
-                t += 1
-                a.t = t
+                nonlocal t, run
+                k, run = run, run + 1
+                flag.zero_()
+                if inject[k]:
+                    q, i, bits = where[k]
+                    cell = grads[q].view(torch.int16)[i:i + 1]
+                    saved = cell.clone()
+                    cell.fill_(bits - 0x10000 if bits >= 0x8000 else bits)
+                else:
+                    t += 1  # an injected step is skipped and keeps t
+                a.t = max(t, 1)
                 if e0 is not None:
                     e0.record(stream)
                 zdp.zdp_step(a, stream)
                 if e1 is not None:
                     e1.record(stream)
+                if inject[k]:
+                    cell.copy_(saved)
+                flags[k:k + 1].copy_(flag)
 
             for _ in range(args.warmup):
                 one()
@@ -796,11 +823,13 @@ def run_sweep(args):
             cold = sorted(e0.elapsed_time(e1) for e0, e1 in ev[:reps])[reps // 2]
             warm = sorted(e0.elapsed_time(e1) for e0, e1 in ev[reps:])[reps // 2]
             nbytes = (4 * P + 32) * n
+            got = flags.cpu().numpy()
             print(json.dumps({"sweep": "fp16_checked_step", "P": P, "n": n,
                               "us_cold": cold * 1e3, "us_warm": warm * 1e3,
                               "GBps_cold": nbytes / cold / 1e6, "GBps_warm": nbytes / warm / 1e6,
-                              "bytes_per_step": nbytes,
-                              "overflow_flag": int(words[0:4].view(torch.int32).item())}),
+                              "bytes_per_step": nbytes, "runs": runs,
+                              "injected_runs": int(inject.sum()),
+                              "flags_match_injections": bool(np.array_equal(got != 0, inject))}),
                   flush=True)
             del grads, st, reps_buf, ws, keep
             torch.cuda.empty_cache()
