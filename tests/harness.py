@@ -87,6 +87,24 @@ def assert_bf16_close(got: np.ndarray, want: np.ndarray, what: str) -> int:
     return worst
 
 
+def assert_bf16_same(got: np.ndarray, want: np.ndarray, what: str):
+    """bf16 bit patterns equal, except that a NaN matches any NaN: IEEE 754
+    leaves the sign and payload of a NaN made by an invalid operation to the
+    implementation (the GPU's conversion writes 0x7FFF, the oracle keeps the
+    sign of its host's NaN with 0x7FC0)."""
+    got = np.asarray(got, np.uint16)
+    want = np.asarray(want, np.uint16)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    nan_g = ((got & 0x7F80) == 0x7F80) & ((got & 0x7F) != 0)
+    nan_w = ((want & 0x7F80) == 0x7F80) & ((want & 0x7F) != 0)
+    assert np.array_equal(nan_g, nan_w), f"{what}: NaN positions differ"
+    bad = (got != want) & ~nan_w
+    if bad.any():
+        i = int(np.flatnonzero(bad.ravel())[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} differ; first at {i}: "
+                             f"got {got.ravel()[i]:#06x} want {want.ravel()[i]:#06x}")
+
+
 class DeviceStep:
     """Device buffers of one step problem: P gradients (bf16/fp16), fp32
     master/m/v of n_pad elements, P bf16 replicas, flag and sum of squares."""
