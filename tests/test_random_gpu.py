@@ -12,8 +12,9 @@ fused step the generator chooses:
 - injected infinities and NaNs;
 - t from 1 to 1000.
 
-The literal ring schedule and the ZeRO++ step get the same treatment: block-aligned
-sub-ranges, extreme block scales and infinite scales for ZeRO++.  Master, fp32
+The literal ring schedule, the unfused chain (reduce-scatter, AdamW on a random
+slice of the shards, all-gather) and the ZeRO++ step get the same treatment:
+block-aligned sub-ranges, extreme block scales and infinite scales for ZeRO++.  Master, fp32
 moments, replicas, flag and quantized outputs must match bit for bit (a bf16
 NaN matches any NaN, see assert_bf16_same); the sum of squares agrees within
 1e-9 relative.
@@ -183,6 +184,53 @@ def _zpp_case(rng):
     assert int(words[0:4].view(torch.int32).item()) == flag, label
     if want_ss:
         _sumsq_close(float(words[8:16].view(torch.float64).item()), ss, label)
+
+
+def _unfused_case(rng):
+    P = int(rng.choice(PS))
+    n = _n(rng, P)
+    S = -(-n // P)
+    gdt = oracle.FP16 if rng.random() < 0.3 else oracle.BF16
+    dtype = torch.float16 if gdt == oracle.FP16 else torch.bfloat16
+    scale = 1.0 / (P * (65536.0 if gdt == oracle.FP16 else 1.0))
+    sh = int(rng.integers(2))  # 1: every buffer one element off 16-byte alignment
+    gbits, w, m, v = random_problem(P, n, int(rng.integers(1 << 30)), gdt)
+    if rng.random() < 0.2:
+        gbits[int(rng.integers(P)), int(rng.integers(n))] = 0x7C00 if gdt == oracle.FP16 else 0x7F80
+    g_dev = [torch.from_numpy(np.concatenate([np.zeros(sh, np.uint16), gbits[q]]).view(np.int16))
+             .to(DEV).view(dtype)[sh:] for q in range(P)]
+    shards = torch.empty(P * S + sh, dtype=torch.float32, device=DEV)[sh:]
+    words = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    zdp.zdp_reduce_scatter(g_dev, shards, n, P, scale, d_overflow=words[0:4].view(torch.int32),
+                           d_sumsq=words[8:16].view(torch.float64))
+    want, flag, ss = oracle.reduce_scatter(gbits, gdt, n, scale, want_sumsq=True)
+    label = f"unfused P={P} n={n} gdt={gdt} shifted={sh}"
+    assert_bits_equal(shards.cpu().numpy(), want, f"{label} shards")
+    assert int(words[0:4].view(torch.int32).item()) == flag, label
+    _sumsq_close(float(words[8:16].view(torch.float64).item()), ss, label)
+    # AdamW on a random slice of the shards, then the all-gather of the master
+    lo = int(rng.integers(0, P * S))
+    count = int(rng.integers(0, P * S - lo + 1))
+    t = int(rng.choice([1, 5, 1000]))
+    st = torch.from_numpy(np.stack([w, m, v])).to(DEV)
+    zdp.zdp_adamw_shard(st[0, lo:], st[1, lo:], st[2, lo:], shards[lo:], count, t=t, **HP)
+    ww, mm, vv = w.copy(), m.copy(), v.copy()
+    if count:
+        ww[lo:lo + count], mm[lo:lo + count], vv[lo:lo + count] = oracle.adamw(
+            w[lo:lo + count], m[lo:lo + count], v[lo:lo + count], want[lo:lo + count], t=t, **HP)
+    for x, y, name in zip(st.cpu().numpy(), (ww, mm, vv), ("master", "m", "v")):
+        assert_bits_equal(x, y, f"{label} adamw [{lo}, {lo + count}) {name}")
+    reps = [torch.empty(n + sh, dtype=torch.bfloat16, device=DEV)[sh:] for _ in range(P)]
+    zdp.zdp_all_gather(st[0], reps, n, P)
+    rep_want = oracle.all_gather(ww, n, P)
+    assert_bf16_same(np.stack([bits_of(r) for r in reps]), rep_want, f"{label} all-gather")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_unfused_chains_match_the_oracle(seed):
+    rng = np.random.default_rng([19, seed])
+    for _ in range(10):
+        _unfused_case(rng)
 
 
 @pytest.mark.parametrize("seed", range(24))
