@@ -303,24 +303,30 @@ def test_finite_gradients_overflowing_fp32():
     _compare_step(dev, w, m, v, rep, 1, None, "fp32 overflow")
 
 
-def test_sum_of_squares_over_extreme_magnitudes():
+@pytest.mark.parametrize("P", [2, 3, 4, 8])
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+def test_sum_of_squares_over_extreme_magnitudes(P, moments):
     # reduced gradients from 1e-30 to 1e30: squares far outside fp32's range
-    # must still add up like the oracle's fp64 sum
-    P, n = 4, 100_003
-    rng = np.random.default_rng(13)
+    # must still add up like the oracle's fp64 sum.  The P and moment types
+    # cover both forms of the fused kernel's range test (per element, and per
+    # vector with its per-element fallback).
+    n = 100_003
+    rng = np.random.default_rng(13 + P)
     vals = (rng.standard_normal((P, n)) * 10.0 ** rng.uniform(-30, 30, (P, n))).astype(np.float32)
     gbits = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    dev = DeviceStep(P, n)
-    dev.load(gbits, np.zeros(dev.n_pad), np.zeros(dev.n_pad), np.zeros(dev.n_pad))
+    dev = DeviceStep(P, n, moments=moments)
+    zeros = np.zeros(dev.n_pad, np.float32 if moments == "f32" else np.uint16)
+    dev.load(gbits, np.zeros(dev.n_pad), zeros, zeros)
+    scale = 1.0 / P
     shards = torch.empty(dev.n_pad, dtype=torch.float32, device="cuda")
-    zdp.zdp_reduce_scatter(dev.grads, shards, n, P, 0.25, dev.flag, dev.sumsq)
-    want, flag, ss = oracle.reduce_scatter(gbits, oracle.BF16, n, 0.25, want_sumsq=True)
+    zdp.zdp_reduce_scatter(dev.grads, shards, n, P, scale, dev.flag, dev.sumsq)
+    want, flag, ss = oracle.reduce_scatter(gbits, oracle.BF16, n, scale, want_sumsq=True)
     assert flag == 0 and int(dev.flag.item()) == 0
     assert np.isfinite(ss) and ss > 1e50
     assert abs(float(dev.sumsq.item()) - ss) <= 1e-9 * ss
     # the same through the fused step
     dev.sumsq.zero_()
-    dev.step(0.25, 3)
+    dev.step(scale, 3)
     assert abs(float(dev.sumsq.item()) - ss) <= 1e-9 * ss
 
 

@@ -46,6 +46,19 @@ inline int fused_cap(int P, int mt) {
   return P < 8 ? 8 : (P < 16 ? 7 : 6);
 }
 
+// Whether the fused step with the sum of squares tests the squares' range per
+// vector (k_fused<..., SQV = true>) rather than per element, for P ranks and
+// the moment type.  Both give the same bits; which is faster depends on the
+// compiled kernel.  Measured on GB300 (time per element / time per vector),
+// fp32 moments: P = 1: 1.016, 2: 0.996, 3: 0.989, 4: 1.018, 5: 0.999, 6:
+// 1.001, 7: 0.994, 8: 1.009, 12: 0.988, 16: 0.987, 24: 0.996, 32: 1.000, 40:
+// 1.011, 48: 1.007, 56: 1.006, 64: 1.005; bf16 moments: P = 2: 1.009, 4:
+// 0.988, 8: 0.989, 64: 1.004.  Chosen where the gain is at least 0.5 %.
+inline bool fused_sqv(int P, int mt) {
+  if (mt != ZDP_MOMENTS_F32) return P == 2;
+  return P == 1 || P == 4 || P == 8 || P == 40 || P == 48 || P == 56 || P == 64;
+}
+
 // Blocks per SM of the reduce-scatter for P ranks; measured fractions of the
 // copy ceiling at the chosen caps: P = 2: 8 blocks, 0.95; P = 4: 16, 0.99
 // (12: 0.96); P = 8, 16, 64: 12, 0.98-0.99.

@@ -356,6 +356,33 @@ struct SumSq {
     lo = 0.0f;
     pending = 0;
   }
+  // The squares of one vector.  When all 8 lie in the compensated range (the
+  // usual case) one branch per vector skips the per-element range tests and
+  // their fp64 fallbacks; the operations on each square are those of add(),
+  // in the same order, so the sum is the same.
+  __device__ __forceinline__ void add_vec(const float (&g)[kVec]) {
+    bool odd = false;
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const float a = fabsf(g[k]);
+      odd |= !(a >= 0x1p-40f && a < 0x1p50f);
+    }
+    if (odd) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) add(g[k]);
+      return;
+    }
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const float p = __fmul_rn(g[k], g[k]);
+      const float e = __fmaf_rn(g[k], g[k], -p);
+      const float s = __fadd_rn(hi, p);
+      const float bp = __fsub_rn(s, hi);
+      const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+      hi = s;
+      lo = __fadd_rn(lo, __fadd_rn(err, e));
+    }
+  }
   // Called once per processed vector.
   __device__ __forceinline__ void tick() {
     if (++pending == 32) flush();
@@ -367,12 +394,19 @@ struct SumSq {
 };
 
 // `sq` is uniform over the grid: whether the caller asked for the sum of squares.
+// SQV: test the squares' range once per vector (SumSq::add_vec) instead of once
+// per element; the same sum, faster or slower depending on the kernel.
+template <bool SQV = false>
 __device__ __forceinline__ void account(const float (&g)[kVec], bool sq, bool& bad, SumSq& ss) {
 #pragma unroll
   for (int k = 0; k < kVec; ++k) bad |= non_finite(g[k]);
   if (sq) {
+    if constexpr (SQV) {
+      ss.add_vec(g);
+    } else {
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) ss.add(g[k]);
+      for (int k = 0; k < kVec; ++k) ss.add(g[k]);
+    }
     ss.tick();
   }
 }
@@ -454,8 +488,8 @@ __device__ __forceinline__ void wait_previous_launch() {
 #endif
 }
 
-// Reduce-scatter + AdamW + cast + all-gather in one pass.
-template <int PT, bool EXACT, int GT, bool VEC>
+// Reduce-scatter + AdamW + cast + all-gather in one pass.  SQV: see account().
+template <int PT, bool EXACT, int GT, bool VEC, bool SQV = false>
 __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KParams p) {
   allow_next_launch();
   const int P = ranks<PT, EXACT>(p);
@@ -476,7 +510,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
         ring_sum_vec<PT, EXACT, GT>(p, P, r, i0, g);
 #pragma unroll
         for (int k = 0; k < kVec; ++k) g[k] = __fmul_rn(g[k], p.scale);
-        account(g, sq, bad, ss);
+        account<SQV>(g, sq, bad, ss);
 #pragma unroll
         for (int k = 0; k < kVec; ++k) adamw(w[k], m[k], v[k], g[k], p.ad);
         st_f8(p.w + i0, w);
