@@ -3,8 +3,9 @@
 Some callers cannot call cudaMalloc: a plug-in running inside a framework
 whose caching allocator owns the device memory, or a step loop that must not
 allocate because cudaMalloc/cudaFree synchronise the device.  For them the
-library keeps the checked step's scratch in its own static device array
-(ZDP_NOALLOC_MAX_LEN elements), so the caller passes only inputs and outputs.
+library keeps the checked step's scratch, in either of its forms, in its own
+static device array (ZDP_NOALLOC_MAX_LEN elements), so the caller passes only
+inputs and outputs.
 
 These tests call it through the C ABI and compare it with zdp_step run with a
 caller workspace: identical results on consecutive calls (the shared scratch
@@ -121,3 +122,27 @@ def test_largest_accepted_range():
         _run(ref, False, t)
         _run(new, True, t)
         _same(ref, new, f"max range, call {t}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("coop", ["1", "0"])
+def test_small_aligned_range_in_both_forms(coop, monkeypatch):
+    # About 100K elements with 16-byte aligned buffers fit one resident wave,
+    # so zdp_step picks the single cooperative launch, which keeps its flag and
+    # barrier counter in the first bytes of the static scratch; ZDP_COOP=0
+    # forces the two passes instead.  Two calls in a row: an infinity (the
+    # update is skipped), then clean gradients (a flag or counter left in the
+    # scratch by the first call would spoil the second).
+    monkeypatch.setenv("ZDP_COOP", coop)
+    P, n = 4, 100_000
+    ref, new = _pair(P, n, seed=41)
+    _new_grads((ref, new), P, n, seed=42, inject=(1, 54_321))
+    _run(ref, False, 1)
+    _run(new, True, 1)
+    assert int(new.flag.item()) == 1
+    _same(ref, new, f"coop={coop} call 1")
+    _new_grads((ref, new), P, n, seed=43)
+    _run(ref, False, 1)
+    _run(new, True, 1)
+    assert int(new.flag.item()) == 0
+    _same(ref, new, f"coop={coop} call 2")

@@ -1,12 +1,15 @@
-// zdp_noalloc.cu -- zdp_step_noalloc: the overflow-checked two-pass step with
-// its scratch in a static device array instead of a caller-provided
-// workspace, for callers that cannot allocate device memory.
+// zdp_noalloc.cu -- zdp_step_noalloc: the overflow-checked step with its
+// scratch in a static device array instead of a caller-provided workspace,
+// for callers that cannot allocate device memory.
 //
-// The scratch holds what the two passes exchange: a 256-byte slot for the
-// device overflow flag, then the reduced gradients of the call's range
-// (len + 8 fp32 values, starting at the multiple of 8 at or below `off`),
-// exactly the layout zdp_step_workspace_bytes() describes.  The array is
-// sized for ZDP_NOALLOC_MAX_LEN elements.
+// The scratch has exactly the layout zdp_step_workspace_bytes() describes: a
+// 256-byte slot whose first 8 bytes hold the device overflow flag (and, for
+// the single cooperative launch, the grid barrier's arrival counter), then,
+// for the two-pass form, the reduced gradients of the call's range (len + 8
+// fp32 values, starting at the multiple of 8 at or below `off`).  The array
+// is sized for ZDP_NOALLOC_MAX_LEN elements.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -23,36 +26,98 @@ constexpr size_t kScratchBytes =
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 256;
+// The context handle and its process-unique id come from the driver API,
+// reached through the runtime's entry-point query so that the library does
+// not link the driver library directly.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch on the current device.  Looked up once per
-// device, with that device current, and cached; the first lookup on a device
+struct DriverEntryPoints {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const DriverEntryPoints& driver_entry_points() {
+  static const DriverEntryPoints eps = [] {
+    DriverEntryPoints d;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      d.get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      d.get_id = reinterpret_cast<CtxGetIdFn>(f);
+    cudaGetLastError();  // a failed query leaves nothing sticky behind
+    return d;
+  }();
+  return eps;
+}
+
+// Process-unique id of the calling thread's current CUDA context; 0 when no
+// context is current yet or the driver cannot tell.  Context handles can be
+// reused after a context is destroyed; these ids are never reused.
+unsigned long long current_context_id() {
+  const DriverEntryPoints& d = driver_entry_points();
+  if (!d.get_current || !d.get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (d.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (d.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+int lookup_failed(cudaError_t e) {
+  char msg[200];
+  std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  return zdp::report_error(ZDP_ERR_CUDA, msg);
+}
+
+// Device address of the scratch in the current context.  Each context that
+// loads this library's module (normally the primary context of a device)
+// holds its own instance of the array, so the address is looked up with
+// cudaGetSymbolAddress once per context, with that context current, and
+// cached under the context's unique id.  A context created later on the same
+// device, after cudaDeviceReset or as a separate (e.g. green) context, gets
+// its own lookup instead of a stale address.  The first lookup in a context
 // may load the library's module there.
 int scratch_address(void** out) {
+  constexpr int kSlots = 64;
   static std::mutex mu;
-  static void* addr[kMaxDevices] = {nullptr};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    char msg[200];
-    std::snprintf(msg, sizeof msg, "cudaGetDevice: %s", cudaGetErrorString(e));
-    return zdp::report_error(ZDP_ERR_CUDA, msg);
-  }
-  if (dev < 0 || dev >= kMaxDevices)
-    return zdp::report_error(ZDP_ERR_CUDA, "device ordinal outside the scratch table");
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      char msg[200];
-      std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress(scratch): %s",
-                    cudaGetErrorString(e));
-      return zdp::report_error(ZDP_ERR_CUDA, msg);
+  static unsigned long long ids[kSlots] = {0};
+  static void* addrs[kSlots] = {nullptr};
+  static int next = 0;
+
+  unsigned long long id = current_context_id();
+  void* p = nullptr;
+  if (id == 0) {
+    // No context is current on this thread yet: the lookup binds the current
+    // device's primary context, whose id can then be read.
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return lookup_failed(e);
+    id = current_context_id();
+    if (id == 0) {  // the driver does not report context ids: no caching
+      *out = p;
+      return ZDP_OK;
     }
-    addr[dev] = p;
   }
-  *out = addr[dev];
+  std::lock_guard<std::mutex> lock(mu);
+  for (int k = 0; k < kSlots; ++k) {
+    if (ids[k] == id) {
+      *out = addrs[k];
+      return ZDP_OK;
+    }
+  }
+  if (p == nullptr) {
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return lookup_failed(e);
+  }
+  ids[next] = id;
+  addrs[next] = p;
+  next = (next + 1) % kSlots;
+  *out = p;
   return ZDP_OK;
 }
 
