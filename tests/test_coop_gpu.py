@@ -97,3 +97,23 @@ def test_barrier_timeout_is_reported_and_writes_nothing(monkeypatch):
     ref = _run(P, n, gbits, w, m, v, rep, coop=False, monkeypatch=monkeypatch)
     assert int(ok.flag.item()) == 0
     _same(ok, ref, "after timeout")
+
+
+@pytest.mark.parametrize("inject", [False, True])
+def test_refused_cooperative_launch_falls_back_to_two_passes(inject, monkeypatch):
+    # A cooperative grid far larger than a resident wave (65,536 blocks more)
+    # is refused by the runtime before anything runs; the call must then take
+    # the two passes and return normally, with the two-pass form's results.
+    # (Had the launch been accepted, its barrier could not be met: it would
+    # time out and the flag would read 2.)
+    P, n = 8, 100_000
+    gbits, w, m, v = random_problem(P, n, 17, oracle.FP16)
+    if inject:
+        gbits[2, 777] = 0xFC00  # -inf
+    rep = np.full((P, n), 0x3F80, np.uint16)
+    monkeypatch.setenv("ZDP_TEST_COOP_OVERSIZE", "65536")
+    a = _run(P, n, gbits, w, m, v, rep, coop=True, monkeypatch=monkeypatch)
+    monkeypatch.delenv("ZDP_TEST_COOP_OVERSIZE")
+    b = _run(P, n, gbits, w, m, v, rep, coop=False, monkeypatch=monkeypatch)
+    assert int(a.flag.item()) == (1 if inject else 0)
+    _same(a, b, f"fallback inject={inject}")
