@@ -86,8 +86,11 @@ enum {
 
 /* Bits of the d_overflow word. */
 #define ZDP_FLAG_OVERFLOW 1 /* some reduced gradient was not finite */
-#define ZDP_FLAG_TIMEOUT 2  /* the single-pass checked step's grid barrier timed out: the
-                               blocks that gave up wrote nothing (see zdp_step) */
+#define ZDP_FLAG_TIMEOUT 2  /* the single-pass checked step's grid barrier timed out.  The
+                               range's master, m, v and replicas are then unspecified (some
+                               blocks may have written their part, others not): the caller
+                               must restore them, e.g. from a copy, before the next step
+                               (see zdp_step) */
 
 /* Library version, e.g. 100 for 0.1.0. */
 int zdp_version(void);
@@ -185,12 +188,22 @@ size_t zdp_step_workspace_bytes(const zdp_step_args* args);
  * registers of one resident wave (about 2 million elements on a GB300), it
  * instead makes one cooperative launch that keeps them in registers across a
  * grid barrier (same results, 8 fewer bytes per element and one launch
- * instead of two).  That barrier waits at most ZDP_COOP_TIMEOUT_NS
+ * instead of two).  If the device cannot run that launch (e.g. fewer SMs are
+ * available to the process than the device reports), the call falls back to
+ * the two passes.  That barrier waits at most ZDP_COOP_TIMEOUT_NS
  * nanoseconds (environment variable, default 1e9); a block that gives up
- * writes nothing and ORs ZDP_FLAG_TIMEOUT into *d_overflow.  Environment
+ * writes nothing of its part of the range and ORs ZDP_FLAG_TIMEOUT into
+ * *d_overflow, while blocks whose wait ended in time go on and write theirs.
+ * So after a timeout the range's master, m, v and replicas are unspecified,
+ * a mix of old and new values, whatever the overflow bit says: the caller
+ * must restore them (from a copy taken before the call, or a checkpoint) and
+ * may rerun the step.  The barrier only times out if the GPU is preempted or
+ * shared so heavily that the resident blocks stop making progress.  Environment
  * variable ZDP_COOP=0 selects the two-pass form always, and
  * ZDP_TEST_COOP_EXTRA_ARRIVALS=k (tests only) makes the barrier wait for k
- * arrivals that never come.  The skip decision covers this call's
+ * arrivals that never come, and ZDP_TEST_COOP_OVERSIZE=k (tests only) asks
+ * for a cooperative grid k blocks larger than one resident wave, which the
+ * runtime refuses, so that the two-pass fallback runs.  The skip decision covers this call's
  * range only; a caller streaming one step through several calls and wanting
  * a step-wide skip must check every range first (e.g. with
  * zdp_reduce_scatter into a scratch buffer).  A skipped step leaves t to the
@@ -224,7 +237,10 @@ int zdp_step_ring(const zdp_step_args* args, void* stream);
  * consecutive elements, global element i in block i / 256.  A block's scale
  * is max|x| / 127 (fp32), q = x / scale rounded half to even and clamped to
  * [-127, 127]; an all-zero block has scale 0; x is recovered as q * scale in
- * fp32.  Non-finite values give unspecified q. */
+ * fp32.  A block holding a NaN has a NaN scale and one holding an infinity
+ * (and no NaN) an infinite scale; a NaN quotient x / scale gives q = -127.
+ * Such a block dequantizes to non-finite values, so a non-finite gradient
+ * that reaches the quantized reduce-scatter raises the overflow flag. */
 #define ZDP_QBLOCK 256
 
 /* Quantize n values (xdt: ZDP_BF16, ZDP_FP16 or ZDP_F32) into q (n int8)
@@ -284,16 +300,21 @@ int zdp_step_zpp(const zdp_zpp_args* args, void* stream);
  * or a step loop that must not call cudaMalloc/cudaFree because they
  * synchronise the device.
  *   args  as for zdp_step; check_overflow, workspace and workspace_bytes are
- *         ignored: the call always runs the two-pass checked step, and its
- *         scratch is a static device array inside libzdp of 64 MiB + 512 B,
- *         which every GPU that loads the library holds until the process exits.
+ *         ignored.  The call runs the overflow-checked step in whichever form
+ *         zdp_step picks for the range (the single cooperative launch or the
+ *         two passes); both forms keep their scratch (the flag and barrier
+ *         words, and the two-pass form's reduced gradients) in a static device
+ *         array inside libzdp of 64 MiB + 512 B, which every GPU that loads the
+ *         library holds until the process exits.
  *   Returns ZDP_ERR_INVALID (nothing enqueued) when args->len exceeds
  *   ZDP_NOALLOC_MAX_LEN; split longer ranges into several calls.
- * It calls no allocating routine.  Its first call on a device looks up the
- * scratch's device address (which may load the library's module on that
- * device); make that first call before any stream capture.  Every call on a
- * device uses the same scratch, which keeps the last call's contents (the call
- * clears the flag itself): calls that may run at the same time on the GPU, e.g.
+ * It calls no allocating routine.  Its first call in a CUDA context (normally
+ * the first on a device) looks up the scratch's device address in that context
+ * with cudaGetSymbolAddress, which may load the library's module there; make
+ * that first call before any stream capture.  Later calls reuse the address
+ * found for the current context.  Every call in a context uses the same
+ * scratch, which keeps the last call's contents (the call clears its flag and
+ * barrier words itself): calls that may run at the same time on the GPU, e.g.
  * on two streams without an ordering between them, race on it. */
 int zdp_step_noalloc(const zdp_step_args* args, void* stream);
 

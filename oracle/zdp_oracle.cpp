@@ -41,7 +41,10 @@
 //    block i / 256); scale = max|x| / 127 over the block (fp32 division),
 //    q = x / scale rounded half to even and clamped to [-127, 127]; an
 //    all-zero block has scale 0 and q = 0; dequantization is q * scale in
-//    fp32.  The quantized all-gather quantizes the bf16 parameter; a
+//    fp32.  (Not on the page, a reading: a block holding a NaN has a NaN
+//    scale, one holding an infinity an infinite scale, and a NaN quotient is
+//    clamped to -127, so that such a block dequantizes to non-finite values
+//    and the overflow flag reports it.)  The quantized all-gather quantizes the bf16 parameter; a
 //    quantized gradient is dequantized in fp32 before the ring sum;
 //  * with bf16 moments (CS336 Lecture 7 notes, 8.4: everything but the fp32
 //    master weight in BF16, 12 bytes per parameter) m and v are stored in
@@ -50,6 +53,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <limits>
 #include <cstdint>
 #include <cstring>
 #include <vector>
@@ -181,10 +185,14 @@ void adamw_element(float& w, float& m, float& v, float g, const Adam& a) {
 // ---------------------------------------------------------------------------
 constexpr int64_t kQBlock = 256;
 
+// The block's largest magnitude over 127.  A NaN anywhere in the block makes
+// the maximum, and so the scale, NaN; an infinity (and no NaN) makes it
+// infinite.  A non-finite block thus dequantizes to non-finite values.
 float quant_scale(const float* x, int64_t count) {
   float amax = 0.0f;
   for (int64_t k = 0; k < count; ++k) {
     const float a = std::fabs(x[k]);
+    if (std::isnan(a)) return std::numeric_limits<float>::quiet_NaN();
     if (a > amax) amax = a;
   }
   return amax / 127.0f;
@@ -192,7 +200,11 @@ float quant_scale(const float* x, int64_t count) {
 
 int8_t quant_one(float x, float scale) {
   if (scale == 0.0f) return 0;
-  float r = std::nearbyint(x / scale);  // the default rounding mode: half to even
+  const float y = x / scale;
+  // x / NaN, or an infinity over an infinite scale: not a number, which the
+  // clamp to [-127, 127] sends to its lower end.
+  if (std::isnan(y)) return -127;
+  float r = std::nearbyint(y);  // the default rounding mode: half to even
   if (r > 127.0f) r = 127.0f;
   if (r < -127.0f) r = -127.0f;
   return static_cast<int8_t>(r);

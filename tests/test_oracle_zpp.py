@@ -9,6 +9,7 @@ exact in bf16, it must update master/m/v exactly like the bf16 step and
 produce the block quantization of that step's bf16 replicas."""
 
 import numpy as np
+import pytest
 
 from harness_cpu import HP, bf16_bits, random_state
 
@@ -124,3 +125,48 @@ def test_zpp_step_on_a_block_range_equals_the_whole(ora):
                  vb, rqb, rsb, n, lo, hi - lo, 1.0 / P, t=5, base=lo, **HP)
     assert np.array_equal(wb, wa[lo:hi]) and np.array_equal(rqb, rqa[:, lo:hi])
     assert np.array_equal(rsb, rsa[:, 4:9])
+
+
+def test_non_finite_blocks_dequantize_to_non_finite_values(ora):
+    # The page leaves non-finite inputs open; the reading: a NaN makes the
+    # block's maximum (so its scale) NaN, an infinity makes it infinite, and a
+    # NaN quotient takes the clamp's lower end, -127.  Every element of such a
+    # block then dequantizes to a non-finite value (q * NaN, 0 * inf, -127 *
+    # inf), while the other blocks quantize as if nothing happened.
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal(256 * 4).astype(np.float32)
+    clean_q, clean_sc = ora.quantize_blocks(x)
+    x[256 + 17] = np.nan
+    x[512 + 3] = np.inf
+    x[768 + 200] = -np.inf
+    q, sc = ora.quantize_blocks(x)
+    assert np.isnan(sc[1]) and sc[2] == np.inf and sc[3] == np.inf
+    assert (q[256:512] == -127).all()
+    for b, k in ((2, 3), (3, 200)):
+        blk = q[256 * b:256 * (b + 1)]
+        assert blk[k] == -127 and not np.delete(blk, k).any()
+    assert np.array_equal(q[:256], clean_q[:256]) and sc[0] == clean_sc[0]
+    xr = ora.dequantize_blocks(q, sc)
+    assert not np.isfinite(xr[256:]).any() and np.isfinite(xr[:256]).all()
+
+
+@pytest.mark.parametrize("bad", [np.nan, np.inf])
+def test_zpp_step_reports_a_non_finite_gradient(ora, bad):
+    # One rank's gradient holds a NaN or an infinity before quantization: the
+    # block's dequantized values, hence the reduced gradients there, are not
+    # finite and the step's overflow flag is raised; other blocks are unharmed.
+    P, n = 4, 256 * 8
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((P, n)) * 1e-3).astype(np.float32)
+    x[2, 256 * 5 + 9] = bad
+    gq = np.empty((P, n), np.int8)
+    gs = np.empty((P, n // 256), np.float32)
+    for q in range(P):
+        gq[q], gs[q] = ora.quantize_blocks(x[q])
+    w, m, v = random_state(n, rng)
+    rq = np.zeros((P, n), np.int8)
+    rs = np.zeros((P, n // 256), np.float32)
+    flag, _ = ora.step_zpp(gq, gs, w, m, v, rq, rs, n, 0, n, 1.0 / P, t=3, **HP)
+    assert flag == 1
+    assert not np.isfinite(w[256 * 5:256 * 6]).any()
+    assert np.isfinite(w[:256 * 5]).all() and np.isfinite(w[256 * 6:]).all()

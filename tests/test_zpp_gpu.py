@@ -272,3 +272,67 @@ def test_zpp_on_the_1p3b_model_sampled_blocks():
         for q in (0, P - 1):
             assert np.array_equal(_i8(rq[q][lo:hi]), wq[q]), f"block {b} replica {q}"
             assert rs[q][b].item() == wsc[q, 0]
+
+
+@pytest.mark.parametrize("xdt", [zdp.ZDP_F32, zdp.ZDP_BF16, zdp.ZDP_FP16])
+def test_quantizer_on_non_finite_blocks_matches_the_oracle(xdt):
+    # A NaN makes its block's scale NaN and every code -127; an infinity makes
+    # the scale infinite, its own code -127 and the others 0.
+    n = 256 * 6 + 50
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    x[256 + 7] = np.nan
+    x[512 + 255] = np.inf
+    x[768] = -np.inf
+    x[1024 + 3], x[1024 + 4] = np.nan, np.inf
+    x[1536 + 49] = np.nan  # the ragged last block
+    if xdt == zdp.ZDP_F32:
+        dx, vals = torch.from_numpy(x).to(DEV), x
+    else:
+        tdt = torch.bfloat16 if xdt == zdp.ZDP_BF16 else torch.float16
+        xt = torch.from_numpy(x).to(tdt)
+        dx, vals = xt.to(DEV), xt.float().numpy()
+    q = torch.empty(n, dtype=torch.int8, device=DEV)
+    sc = torch.empty(-(-n // 256), dtype=torch.float32, device=DEV)
+    zdp.zdp_quantize_blocks(dx, xdt, n, q, sc)
+    wq, ws = oracle.quantize_blocks(vals)
+    torch.cuda.synchronize()
+    assert np.array_equal(_i8(q), wq)
+    assert_bits_equal(sc.cpu().numpy(), ws, "scales")  # NaN matches NaN
+    assert np.isnan(ws[1]) and ws[2] == np.inf and np.isnan(ws[4]) and np.isnan(ws[6])
+
+
+@pytest.mark.parametrize("bad", [np.nan, np.inf])
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+def test_zpp_step_flags_a_non_finite_gradient(bad, moments):
+    P, n = 8, 256 * 40 + 77
+    gq, gs, w, m, v = _zpp_problem(P, n, 123, moments)
+    x = (np.random.default_rng(9).standard_normal(n) * 1e-3).astype(np.float32)
+    x[256 * 11 + 100] = bad
+    gq[3], gs[3] = oracle.quantize_blocks(x)
+    dg, ds, dw, dm, dv, rq, rs = _to_dev(gq, gs, w, m, v, P, n, moments)
+    words = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    a, keep = zdp.make_zpp_args(dg, ds, dw, dm, dv, rq, rs, n=n, scale=1.0 / P, t=4,
+                                d_overflow=words[0:4].view(torch.int32), moments=moments, **HP)
+    zdp.zdp_step_zpp(a)
+    torch.cuda.synchronize()
+    nb = gs.shape[1]
+    wq, wsc = np.zeros((P, n), np.int8), np.zeros((P, nb), np.float32)
+    ww, mm, vv = w.copy(), m.copy(), v.copy()
+    flag, _ = oracle.step_zpp(gq, gs, ww, mm, vv, wq, wsc, n, 0, n, 1.0 / P, t=4,
+                              moments=moments, **HP)
+    assert flag == 1 and int(words[0:4].view(torch.int32).item()) == 1
+    assert not np.isfinite(ww[256 * 11:256 * 12]).any()
+    assert_state_close(dw.cpu().numpy()[:n], ww[:n], "master")
+    if moments == "f32":
+        assert_state_close(dm.cpu().numpy()[:n], mm[:n], "m")
+        assert_state_close(dv.cpu().numpy()[:n], vv[:n], "v")
+    else:
+        mb, vb = bits_of(dm)[:n], bits_of(dv)[:n]
+        for got, want, name in ((mb, mm[:n], "m"), (vb, vv[:n], "v")):
+            nan_w = ((want & 0x7F80) == 0x7F80) & ((want & 0x7F) != 0)
+            nan_g = ((got & 0x7F80) == 0x7F80) & ((got & 0x7F) != 0)
+            assert np.array_equal(nan_g, nan_w) and np.array_equal(got[~nan_w], want[~nan_w]), name
+    for q in range(P):
+        assert np.array_equal(_i8(rq[q]), wq[q]), f"replica {q}"
+        assert_bits_equal(rs[q].cpu().numpy(), wsc[q], f"replica scales {q}")

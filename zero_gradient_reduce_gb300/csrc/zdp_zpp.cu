@@ -45,7 +45,9 @@ __device__ __forceinline__ float dequant(int8_t q, float scale) {
   return __fmul_rn(__int2float_rn(q), scale);
 }
 
-// Reference form of the code: exact division, round half to even, clamp.
+// Reference form of the code: exact division, round half to even, clamp.  A
+// NaN quotient (x / NaN, or inf / inf) clamps to -127: fmaxf returns its
+// non-NaN operand.
 __device__ __forceinline__ int quant_div(float x, float scale) {
   float r = rintf(__fdiv_rn(x, scale));
   r = fminf(fmaxf(r, -127.0f), 127.0f);
@@ -85,9 +87,15 @@ __device__ __forceinline__ void quant8(const float (&x)[kVec], float scale, int 
   }
 }
 
-// Warp maximum of non-negative floats (their bit patterns order like the values).
-__device__ __forceinline__ float warp_absmax(float a) {
-  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
+// |x| as its bit pattern.  These patterns order like the magnitudes, with
+// every NaN above +inf, so an unsigned maximum over them propagates a NaN
+// (fmaxf would drop it): a block holding a NaN gets a NaN scale, one holding
+// an infinity an infinite scale, and either dequantizes to non-finite values.
+__device__ __forceinline__ uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7fffffffu; }
+
+// Warp maximum of magnitudes given as abs_bits patterns, as a float.
+__device__ __forceinline__ float warp_absmax(uint32_t a) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, a));
 }
 
 __device__ __forceinline__ uint2 pack_i8x8(const int (&q)[kVec]) {
@@ -270,11 +278,10 @@ __global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : Z
         }
       }
     }
-    float amax = 0.0f;
+    uint32_t abits = 0;
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) amax = fmaxf(amax, fabsf(pv[e]));
-    amax = warp_absmax(amax);
-    const float sc = __fdiv_rn(amax, 127.0f);
+    for (int e = 0; e < kVec; ++e) abits = max(abits, abs_bits(pv[e]));
+    const float sc = __fdiv_rn(warp_absmax(abits), 127.0f);
     int qv[kVec];
     quant8(pv, sc, qv);
     if (cnt == kVec) {
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const void* x, int64_t n,
   for (int64_t b = warp; b * kQB < n; b += nwarps) {
     const int64_t i0 = b * kQB + lane * kVec;
     float v[kVec];
-    float amax = 0.0f;
+    uint32_t abits = 0;
 #pragma unroll
     for (int e = 0; e < kVec; ++e) {
       const int64_t i = i0 + e;
@@ -318,10 +325,9 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const void* x, int64_t n,
         }
       }
       v[e] = xv;
-      amax = fmaxf(amax, fabsf(xv));
+      abits = max(abits, abs_bits(xv));
     }
-    amax = warp_absmax(amax);
-    const float sc = __fdiv_rn(amax, 127.0f);
+    const float sc = __fdiv_rn(warp_absmax(abits), 127.0f);
     int qv[kVec];
     quant8(v, sc, qv);
 #pragma unroll
