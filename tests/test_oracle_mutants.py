@@ -109,6 +109,14 @@ MUTANTS = [
     ("ZeRO++ sum of squares skips the owner's rank",
      [(CPP, "vals[q] = dequant_one(gq[q * ld + j], gs[q * sld + i / kQBlock - off / kQBlock]);",
        "vals[q] = q == owner_of(i, S) ? 0.0f : dequant_one(gq[q * ld + j], gs[q * sld + i / kQBlock - off / kQBlock]);")]),
+    # the sampled step (the checker of the full-size parity tests)
+    ("sampled step ignores the skip", [(CPP, "    if (!skip) {", "    if (true) {")]),
+    ("sampled owner from the position in the sample",
+     [(CPP, "ring_sum(vals.data(), P, owner_of(idx[j], S)) * scale;",
+       "ring_sum(vals.data(), P, owner_of(j, S)) * scale;")]),
+    ("sampled step widens every gradient as bf16",
+     [(CPP, "for (int q = 0; q < P; ++q) vals[q] = widen(gs[q * k + j], gdt);",
+       "for (int q = 0; q < P; ++q) vals[q] = widen(gs[q * k + j], 0);")]),
     # replicas
     ("replicas truncated to bf16",
      [(CPP, "const uint16_t p = float_to_bf16_rne(master[k]);",
@@ -125,8 +133,12 @@ MUTANTS = [
        "static_cast<uint16_t*>(base)[k] = static_cast<uint16_t>(float_to_bits(x) >> 16);")]),
     # ZeRO++ block quantization
     ("quantization scale amax/128", [(CPP, "return amax / 127.0f;", "return amax / 128.0f;")]),
-    ("quantization truncates", [(CPP, "std::nearbyint(x / scale);", "std::trunc(x / scale);")]),
-    ("quantization ties away from zero", [(CPP, "std::nearbyint(x / scale);", "std::round(x / scale);")]),
+    ("quantization truncates", [(CPP, "std::nearbyint(y);", "std::trunc(y);")]),
+    ("quantization ties away from zero", [(CPP, "std::nearbyint(y);", "std::round(y);")]),
+    ("quantization drops a NaN from the block maximum",
+     [(CPP, "if (std::isnan(a)) return std::numeric_limits<float>::quiet_NaN();", "")]),
+    ("a NaN quotient clamps to +127", [(CPP, "if (std::isnan(y)) return -127;",
+                                        "if (std::isnan(y)) return 127;")]),
     ("quantization clamps at 126", [(CPP, "if (r > 127.0f) r = 127.0f;", "if (r > 126.0f) r = 126.0f;")]),
     ("dequantization reads the next block's scale",
      [(CPP, "x[i] = dequant_one(q[i], scales[i / kQBlock]);",
