@@ -114,7 +114,7 @@ def bytes_per_param(P: int, moments: str = "f32") -> int:
     return 2 * P + state + state + 2 * P
 
 
-def config_of(wl, bucket_elems=0, l2_flush=False):
+def config_of(wl, bucket_elems=0, l2_flush=False, moments="f32", check_overflow=False):
     return {
         "workload": wl.name,
         "n_params": wl.n,
@@ -122,14 +122,25 @@ def config_of(wl, bucket_elems=0, l2_flush=False):
         "shard": -(-wl.n // wl.P),
         "tensors": len(wl.tensors),
         "grad_dtype": wl.grad_dtype,
-        "state": "fp32 master/m/v, bf16 replicas",
+        "state": ("fp32 master/m/v, bf16 replicas" if moments == "f32" else
+                  "fp32 master, bf16 m/v, bf16 replicas"),
         "bucket_elems": bucket_elems,
-        "check_overflow": False,
+        "check_overflow": bool(check_overflow),
+        "moments": moments,
         "outputs": "overflow flag + fp64 grad sum of squares",
         "l2": ("flushed (2x L2 written) before every step; steps timed alone" if l2_flush else
                "no flush: every step streams (4P+24)n bytes, far above the 129 MB L2"),
         "parallelism": "P logical ZeRO ranks in one GPU; replicas per GPU when n_gpus > 1",
     }
+
+
+GB300_L2_BYTES = 129 << 20  # a GB300's L2, about 129 MB (used where no GPU is queried)
+
+
+def step_flushes_l2(wl, moments="f32", l2=GB300_L2_BYTES):
+    """Whether a step of this workload moves so few bytes (under four L2
+    sizes) that it is timed alone after a flush of the L2."""
+    return bytes_per_param(wl.P, moments) * wl.n < 4 * l2
 
 
 def measured_peak():
@@ -341,7 +352,7 @@ def run_ours(args):
     # launches alone with events.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = (torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-             if bytes_per_param(P, args.moments) * n < 4 * l2 else None)
+             if step_flushes_l2(wl, args.moments, l2) else None)
     t = 0
 
     def one_step(e0=None, e1=None):
@@ -428,8 +439,8 @@ def run_ours(args):
             "dtype": "f32",
             "data": "synthetic: seeded N(0, sigma_T) bf16 gradients (sigma_T log-uniform "
                     "[1e-5, 1e-2] per tensor), master ~ N(0, 0.02), m = v = 0 at t = 1",
-            "config": dict(config_of(wl, wl.bucket_elems, flush is not None),
-                           moments=args.moments, check_overflow=bool(args.check_overflow)),
+            "config": config_of(wl, wl.bucket_elems, flush is not None, args.moments,
+                                args.check_overflow),
             "hbm_tbs": alg_bytes / (ms_per_step / 1e3) / 1e12,
             "roofline": {
                 "bound": "hbm",
@@ -699,10 +710,14 @@ def run_reference(args):
     oracle.build()
     t = 0
 
+    if args.moments == "bf16":  # the moments held in bf16 (zeros either way)
+        m, v = np.zeros(length, np.uint16), np.zeros(length, np.uint16)
+
     def step():
         nonlocal t
         t += 1
-        oracle.step(g, oracle.BF16, w, m, v, rep, n, lo, length, wl.scale, t=t, base=lo, **HP)
+        oracle.step(g, oracle.BF16, w, m, v, rep, n, lo, length, wl.scale, t=t, base=lo,
+                    moments=args.moments, check_overflow=args.check_overflow, **HP)
 
     for _ in range(args.warmup):
         step()
@@ -711,8 +726,8 @@ def run_reference(args):
         step()
     el = time.perf_counter() - t0
     value = args.steps * length / el
-    sample = (f"each step: one oracle step over params [{lo}, {lo + length}) of {wl.name} "
-              f"(P={P}), single-threaded")
+    sample = (f"each step: one oracle step over the {length} params [{lo}, {lo + length}) of "
+              f"{wl.name} (P={P}, straddling the rank 0/1 shard boundary), single-threaded")
     print(json.dumps({
         "impl": "reference",
         "metric": METRIC,
@@ -721,13 +736,18 @@ def run_reference(args):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": el / args.steps * 1e3 * (n / length),
+        # the measured time of one step as run (one oracle step over the sample)
+        "ms_per_step": el / args.steps * 1e3,
+        "params_per_step": length,
+        # the same per-parameter rate carried to one step over all n parameters
+        "extrapolated_full_step_ms": el / args.steps * 1e3 * (n / length),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic: seeded bf16 gradients and fp32 state of the same distributions",
-        "config": config_of(wl),
+        "config": config_of(wl, wl.bucket_elems, step_flushes_l2(wl, args.moments),
+                            args.moments, args.check_overflow),
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
                          "host_cores": os.cpu_count(), "sample": sample},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
