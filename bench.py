@@ -81,6 +81,14 @@ def parse_args():
                     help="time the overflow-checked step (skip on a non-finite reduced "
                          "gradient): one cooperative launch when the range fits one resident "
                          "wave, else two passes through a workspace")
+    ap.add_argument("--overlap", action="store_true",
+                    help="the ZeRO-2 streamed step: a producer stream writes each bucket's "
+                         "gradients while zdp_step runs on the previous bucket on a second "
+                         "stream; overlapped, producer-alone and step-alone times (default "
+                         "workload of this mode: the 7B model in 256 MiB buckets)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="skip the ZeRO-2 streamed-step overlap measurement (7B model) that the "
+                         "default run adds to its line")
     ap.add_argument("--unfused", action="store_true",
                     help="the three-call chain zdp_reduce_scatter -> zdp_adamw_shard -> "
                          "zdp_all_gather against the fused step, per-stage times: one JSON line")
@@ -473,9 +481,37 @@ def run_ours(args):
                                   "bytes per parameter than the algorithmic bytes above")
         if world == 1 and not args.no_cpu_baseline and not args.check_overflow:
             out["cpu_baseline"] = cpu_baseline(args, wl, grads, master, m, v, P, n)
-        if wl.name != workloads.gpt_1p3b().name:
-            note = f"measured on the {wl.name} workload, not the 1.3B headline"
-            out["metric_note"] = note + ("; " + out["metric_note"] if "metric_note" in out else "")
+    # The ZeRO-2 streamed step of the 7B model, overlapped with its gradient
+    # producer on a second stream (every rank runs it on its own GPU; rank 0's
+    # figures are reported).  The headline buffers are freed first: the 7B
+    # state and replicas take 184 GB.
+    overlap = None
+    if (not args.no_overlap and wl.name == workloads.gpt_1p3b().name
+            and args.moments == "f32" and not args.check_overflow):
+        del a, keep, grads, state, master, m, v, replicas, ws
+        torch.cuda.empty_cache()
+        o = overlap_measure(workloads.gpt_7b(), dev, seed, steps=3, warmup=2)
+        if rank == 0:
+            peak, peak_kind = measured_peak()
+            gbs = lambda ms: o["step_bytes"] / (ms / 1e3) / 1e9  # noqa: E731
+            overlap = {
+                "workload": workloads.gpt_7b().name,
+                "what": ("zdp_step per 256 MiB bucket on one stream while the producer draws the "
+                         "next bucket's gradients on another (two bucket buffers)"),
+                "wall_ms": o["wall_ms"], "wall_ms_each": o["wall_ms_each"],
+                "producer_alone_ms": o["producer_alone_ms"],
+                "step_alone_ms": o["step_alone_ms"], "sum_alone_ms": o["sum_alone_ms"],
+                "hidden_ms": o["hidden_ms"],
+                "step_under_contention_ms": o["step_under_contention_ms"],
+                "step_alone_frac": gbs(o["step_alone_ms"]) / peak,
+                "step_under_contention_frac": gbs(o["step_under_contention_ms"]) / peak,
+                "peak_source": f"{peak_kind} HBM copy bandwidth", "steps": 3,
+                "overflow_flag": o["overflow_flag"]}
+    if out is not None and overlap is not None:
+        out["streamed_overlap"] = overlap
+    if out is not None and wl.name != workloads.gpt_1p3b().name:
+        note = f"measured on the {wl.name} workload, not the 1.3B headline"
+        out["metric_note"] = note + ("; " + out["metric_note"] if "metric_note" in out else "")
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -1075,6 +1111,137 @@ def run_unfused(args):
     }), flush=True)
 
 
+def overlap_measure(wl, dev, seed, steps, warmup, stream_times=True):
+    """The ZeRO-2 streamed step of `wl` (its buckets; 256 MiB per rank when it
+    has none) driven by zero_gradient_reduce_gb300.streaming: the producer
+    (the seeded gradient generator, standing in for the backward pass) on one
+    stream, zdp_step on another, two bucket buffers.  Returns a dict of mean
+    ms per step: overlapped wall time (start of the step to the last bucket's
+    update), the producer alone, the steps alone (back to back on the step
+    stream), and the zdp_step launches' own time inside the overlapped run
+    (under contention with the producer), with the step's algorithmic bytes."""
+    import torch
+
+    from zero_gradient_reduce_gb300 import streaming, workloads, zdp
+
+    P, n = wl.P, wl.n
+    S = -(-n // P)
+    B = wl.bucket_elems or (128 << 20)
+    state = [torch.empty(P * S, dtype=torch.float32, device=dev) for _ in range(3)]
+    workloads.fill_state(state[0], state[1], state[2], wl, seed)
+    replicas = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    words = torch.zeros(16, dtype=torch.uint8, device=dev)
+    ss = streaming.StreamedStep(P, n, B, state[0], state[1], state[2], replicas,
+                                scale=wl.scale, d_overflow=words[0:4].view(torch.int32),
+                                d_sumsq=words[8:16].view(torch.float64), device=dev, **HP)
+    nb = len(ss.bounds)
+    gen_step = 0
+
+    def produce(views, lo, hi):
+        for q in range(P):
+            workloads.fill_bucket_grads(views[q], wl, q, gen_step, seed, lo)
+
+    t = wl.t0
+    for _ in range(warmup):
+        words.zero_()
+        ss.run(t, produce)
+        t += 1
+        gen_step += 1
+    torch.cuda.synchronize()
+    times = [streaming.StepTimes(nb) for _ in range(steps)]
+    for k in range(steps):
+        words.zero_()
+        ss.run(t, produce, times[k])
+        t += 1
+        gen_step += 1
+    torch.cuda.synchronize()
+    flag = int(words[0:4].view(torch.int32).item())
+    wall = sum(x.wall_ms() for x in times) / steps
+    under = sum(x.step_ms() for x in times) / steps
+
+    def alone(stream, body):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            body()  # warm-up
+            for e0, e1 in ev:
+                e0.record(stream)
+                body()
+                e1.record(stream)
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+
+    def producer_only():
+        for b, (lo, hi) in enumerate(ss.bounds):
+            produce(ss.views(b), lo, hi)
+
+    def steps_only():  # the buckets' last contents: finite gradients, same work
+        for a, _ in ss.args:
+            zdp.zdp_step(a, ss.stepper)
+
+    prod_ms = alone(ss.producer, producer_only)
+    step_ms = alone(ss.stepper, steps_only)
+    out = {"buckets": nb, "bucket_elems": B, "wall_ms": wall,
+           "wall_ms_each": [x.wall_ms() for x in times], "producer_alone_ms": prod_ms,
+           "step_alone_ms": step_ms, "sum_alone_ms": prod_ms + step_ms,
+           "hidden_ms": prod_ms + step_ms - wall, "step_under_contention_ms": under,
+           "step_bytes": bytes_per_param(P) * n, "overflow_flag": flag,
+           "producer": "seeded N(0, sigma) bf16 gradients drawn bucket by bucket "
+                       "(workloads.fill_bucket_grads: one torch normal_ per rank and tensor "
+                       "slice), standing in for the backward pass"}
+    del ss, state, replicas
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_overlap(args):
+    import torch
+
+    from zero_gradient_reduce_gb300 import workloads, zdp
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    zdp.load()
+    name = args.workload if args.workload != "gpt_1p3b" else "gpt_7b"
+    wl = workloads.by_name(name)
+    sampler = ClockSampler(gpu_id_for_smi(local_rank))
+    sampler.start()
+    wall0 = time.time()
+    o = overlap_measure(wl, dev, args.seed + 1000 * rank, args.steps, args.warmup)
+    wall1 = time.time()
+    sampler.stop()
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    n = wl.n
+
+    def frac(ms):
+        return o["step_bytes"] / (ms / 1e3) / 1e9 / peak
+
+    print(json.dumps({
+        "metric": METRIC, "value": n / (o["wall_ms"] / 1e3), "unit": "params/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": o["wall_ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded bf16 gradients drawn bucket by bucket by the producer",
+        "config": dict(config_of(wl, o["bucket_elems"]),
+                       l2="each bucket's gradients written by the producer just before its step",
+                       streaming="two streams, two bucket buffers"),
+        "overlap": dict(o, step_alone_frac=frac(o["step_alone_ms"]),
+                        step_under_contention_frac=frac(o["step_under_contention_ms"]),
+                        peak=peak, peak_source=f"{peak_kind} HBM copy bandwidth"),
+        "gpu_launches": args.steps * o["buckets"],
+        "clocks": sampler.summary(wall0, wall1),
+        "metric_note": (f"the ZeRO-2 streamed step of {wl.name} overlapped with its gradient "
+                        "producer: value and ms_per_step are the overlapped wall time"),
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -1087,6 +1254,8 @@ def main():
         run_ring_study(args)
     elif args.unfused:
         run_unfused(args)
+    elif args.overlap:
+        run_overlap(args)
     else:
         run_ours(args)
 

@@ -15,7 +15,7 @@ import numpy as np
 import torch
 
 import oracle
-from zero_gradient_reduce_gb300 import zdp
+from zero_gradient_reduce_gb300 import workloads, zdp
 
 STATE_RTOL = 1e-6
 STATE_ATOL_FLOOR = 1e-30
@@ -198,3 +198,34 @@ def random_problem(P, n, seed, gdt=oracle.BF16, fresh=False, grad_scale=1e-3):
         m[:n] = rng.standard_normal(n) * 1e-4
         v[:n] = rng.uniform(0, 1e-6, n)
     return np.ascontiguousarray(gbits), w, m, v
+
+
+class SampledProducer:
+    """produce() callback: writes the seeded gradients of a bucket and keeps
+    the values at the sampled indices that fall in it (on the producer
+    stream, right after writing them)."""
+
+    def __init__(self, wl, seed, idx, P, fill=workloads.fill_grads):
+        self.wl, self.seed, self.P, self.fill = wl, seed, P, fill
+        self.idx = idx
+        self.gs = torch.zeros((P, idx.size), dtype=torch.int16, device="cuda")
+        self.step = 0
+
+    def prepare(self, bounds):
+        self.sel = []
+        for lo, hi in bounds:
+            k = np.nonzero((self.idx >= lo) & (self.idx < hi))[0]
+            self.sel.append((torch.from_numpy(k).cuda(),
+                             torch.from_numpy(self.idx[k] - lo).cuda()))
+        torch.cuda.synchronize()
+        self.bounds = bounds
+
+    def __call__(self, views, lo, hi):
+        b = self.bounds.index((lo, hi))
+        pos, local = self.sel[b]
+        for q in range(self.P):
+            self.fill(views[q], self.wl, q, self.step, self.seed, lo)
+            self.gs[q].index_copy_(0, pos, views[q].view(torch.int16).index_select(0, local))
+
+    def host_values(self):
+        return self.gs.cpu().numpy().view(np.uint16)

@@ -25,8 +25,9 @@ import pytest
 import torch
 
 import oracle
-from harness import HP, assert_bf16_close, assert_bits_equal, assert_state_close, bits_of
-from zero_gradient_reduce_gb300 import workloads, zdp
+from harness import (HP, SampledProducer, assert_bf16_close, assert_bits_equal,
+                     assert_state_close, bits_of)
+from zero_gradient_reduce_gb300 import streaming, workloads, zdp
 
 pytestmark = pytest.mark.gpu
 
@@ -174,38 +175,31 @@ def test_gpt_1p3b_bench_configuration(moments):
 
 def test_gpt_7b_streamed_buckets():
     # fp32 state (79 GB) and 8 replicas (105 GB) resident; each rank's
-    # gradients regenerated one 256 MiB bucket at a time and streamed
-    # through zdp_step with off/len
+    # gradients regenerated one 256 MiB bucket at a time by a producer stream
+    # into two bucket buffers, while zdp_step (off/len) runs on the previous
+    # bucket on a second stream: the ZeRO-2 streamed step, overlapped
     wl = workloads.gpt_7b()
     seed = 4
     pb = Problem(wl, seed, grads=False)
     B = wl.bucket_elems
-    bucket = [torch.empty(B, dtype=torch.bfloat16, device=DEV) for _ in range(pb.P)]
     idx = sample_indices(pb.n, pb.S, pb.P, seed,
                          extra=list(range(0, pb.n, B)) + [t.offset for t in wl.tensors],
                          k_random=50_000, around=4)
     idx_dev = torch.from_numpy(idx).to(DEV)
     w, m, v = pb.oracle_state(idx_dev)
-    gs = np.empty((pb.P, idx.size), np.uint16)
-    for lo in range(0, pb.n, B):
-        hi = min(pb.n, lo + B)
-        for q in range(pb.P):
-            workloads.fill_grads(bucket[q][:hi - lo], wl, q, 0, seed, lo)
-        sel = (idx >= lo) & (idx < hi)
-        local = torch.from_numpy(idx[sel] - lo).to(DEV)
-        for q in range(pb.P):
-            gs[q, sel] = gather_bits(bucket[q], local)
-        args, keep = zdp.make_step_args([b[:hi - lo] for b in bucket], pb.state[0], pb.state[1],
-                                        pb.state[2], pb.replicas, n=pb.n, scale=wl.scale,
-                                        t=wl.t0, off=lo, length=hi - lo, d_overflow=pb.flag,
-                                        d_sumsq=pb.sumsq, **HP)
-        zdp.zdp_step(args)
-        torch.cuda.synchronize()  # the bucket buffers are refilled next
-    gout, rep, flag = oracle.step_sampled(gs, idx, oracle.BF16, w, m, v, pb.n, wl.scale,
-                                          t=wl.t0, **HP)
+    ss = streaming.StreamedStep(pb.P, pb.n, B, pb.state[0], pb.state[1], pb.state[2],
+                                pb.replicas, scale=wl.scale, d_overflow=pb.flag,
+                                d_sumsq=pb.sumsq, **HP)
+    prod = SampledProducer(wl, seed, idx, pb.P)
+    prod.prepare(ss.bounds)
+    prod.step = 0
+    ss.run(wl.t0, prod)
+    torch.cuda.synchronize()
+    gout, rep, flag = oracle.step_sampled(prod.host_values(), idx, oracle.BF16, w, m, v, pb.n,
+                                          wl.scale, t=wl.t0, **HP)
     assert flag == 0 and int(pb.flag.item()) == 0
     pb.check(idx, idx_dev, w, m, v, rep, "7B streamed")
-    del pb, bucket
+    del pb, ss, prod
     _free()
 
 

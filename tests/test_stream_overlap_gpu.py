@@ -1,73 +1,101 @@
-"""ZeRO-2-style streaming (CS336 Lecture 7 notes, 8.2: gradients reduced bucket by
-bucket as the backward pass produces them, and freed): a producer stream writes
-each bucket's P gradient slices into one of two bucket buffers while zdp_step
-runs on the previous bucket on a second stream.  Events order the two streams
-(ready: producer -> step; done: step -> producer before the buffer is reused).
-Ownership is global, so the streamed step must equal one whole-model call bit
-for bit, whatever the interleaving."""
+"""ZeRO-2 streaming (CS336 Lecture 7 notes, 8.2 items 1-4: each bucket's
+gradients are reduce-scattered as soon as the backward pass produces them,
+then freed, and every rank updates the shard it owns; 6.4: buckets overlapped
+with the backward pass).  A producer stream writes each bucket's P gradient
+slices into one of two bucket buffers while zdp_step runs on the previous
+bucket on a second stream (zero_gradient_reduce_gb300.streaming).
+
+Checked two ways: against the oracle at sampled global indices (every bucket,
+shard and tensor boundary with neighbours, and random elements) over
+consecutive steps of the GPT-2-small-shaped model, and against one
+whole-model zdp_step call, bit for bit, on flat models with ragged buckets.
+Ownership is global, so no interleaving of the two streams may change a bit.
+"""
 
 import numpy as np
 import pytest
 import torch
 
-from harness import HP, assert_bits_equal, bits_of
-from zero_gradient_reduce_gb300 import workloads, zdp
+import oracle
+from harness import HP, SampledProducer, assert_bits_equal, bits_of
+from test_parity_full_gpu import Problem, _free, sample_indices
+from zero_gradient_reduce_gb300 import streaming, workloads, zdp
 
 pytestmark = pytest.mark.gpu
 
 
-def _state(wl, seed):
-    P, n = wl.P, wl.n
-    S = -(-n // P)
-    st = [torch.empty(P * S, dtype=torch.float32, device="cuda") for _ in range(3)]
-    workloads.fill_state(st[0], st[1], st[2], wl, seed)
-    reps = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-    words = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    return st, reps, words
+def test_gpt2_small_streamed_on_two_streams_matches_the_oracle():
+    wl = workloads.gpt2_small()
+    seed = 6
+    pb = Problem(wl, seed, grads=False)
+    B = wl.bucket_elems
+    idx = sample_indices(pb.n, pb.S, pb.P, seed,
+                         extra=list(range(0, pb.n, B)) + [t.offset for t in wl.tensors],
+                         k_random=30_000, around=8)
+    idx_dev = torch.from_numpy(idx).to("cuda")
+    w, m, v = pb.oracle_state(idx_dev)
+    ss = streaming.StreamedStep(pb.P, pb.n, B, pb.state[0], pb.state[1], pb.state[2],
+                                pb.replicas, scale=wl.scale, d_overflow=pb.flag,
+                                d_sumsq=pb.sumsq, **HP)
+    assert len(ss.bounds) > 2
+    # the bucket-wise generator the overlap benchmark uses as its producer
+    prod = SampledProducer(wl, seed, idx, pb.P, fill=workloads.fill_bucket_grads)
+    prod.prepare(ss.bounds)
+    for t in (1, 2, 3):
+        prod.step = t
+        pb.words.zero_()
+        ss.run(t, prod)
+        torch.cuda.synchronize()
+        gout, rep, flag = oracle.step_sampled(prod.host_values(), idx, oracle.BF16, w, m, v,
+                                              pb.n, wl.scale, t=t, **HP)
+        assert flag == 0 and int(pb.flag.item()) == 0
+        pb.check(idx, idx_dev, w, m, v, rep, f"gpt2 two streams t={t}")
+    del pb, ss, prod
+    _free()
 
 
-@pytest.mark.parametrize("P,n,bucket", [(8, 50_000_017, 4_000_037), (4, 9_999_991, 1_000_003)])
-def test_streamed_buckets_on_two_streams_equal_one_call(P, n, bucket):
+@pytest.mark.parametrize("P,n,bucket,nbuf", [(8, 50_000_017, 4_000_037, 2),
+                                             (4, 9_999_991, 1_000_003, 2),
+                                             (3, 3_000_001, 999_999, 3)])
+def test_streamed_buckets_on_two_streams_equal_one_call(P, n, bucket, nbuf):
     wl = workloads.Workload(f"flat_{n}_p{P}", P=P, n=n, tensors=workloads._flat(n), t0=3)
     seed = 11
+    S = -(-n // P)
+
+    def state():
+        st = [torch.empty(P * S, dtype=torch.float32, device="cuda") for _ in range(3)]
+        workloads.fill_state(st[0], st[1], st[2], wl, seed)
+        reps = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        return st, reps, torch.zeros(16, dtype=torch.uint8, device="cuda")
+
     # reference: every rank's whole gradient resident, one call
     grads = [workloads.fill_grads(torch.empty(n, dtype=torch.bfloat16, device="cuda"), wl, q,
                                   0, seed) for q in range(P)]
-    st_ref, reps_ref, words_ref = _state(wl, seed)
+    st_ref, reps_ref, words_ref = state()
     a, keep = zdp.make_step_args(grads, st_ref[0], st_ref[1], st_ref[2], reps_ref, n=n,
-                                 scale=wl.scale, t=wl.t0, d_overflow=words_ref[0:4].view(torch.int32),
-                                 **HP)
+                                 scale=wl.scale, t=wl.t0,
+                                 d_overflow=words_ref[0:4].view(torch.int32),
+                                 d_sumsq=words_ref[8:16].view(torch.float64), **HP)
     zdp.zdp_step(a)
     torch.cuda.synchronize()
 
-    # streamed: two bucket buffers, producer and step on separate streams
-    st, reps, words = _state(wl, seed)
-    bufs = [[torch.empty(bucket, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-            for _ in range(2)]
-    producer, stepper = torch.cuda.Stream(), torch.cuda.Stream()
-    bounds = [(lo, min(n, lo + bucket)) for lo in range(0, n, bucket)]
-    ready = [torch.cuda.Event() for _ in bounds]
-    done = [torch.cuda.Event() for _ in bounds]
-    keep_all = []
-    for b, (lo, hi) in enumerate(bounds):
-        buf = bufs[b % 2]
-        with torch.cuda.stream(producer):
-            if b >= 2:
-                producer.wait_event(done[b - 2])  # the step on this buffer has finished
-            for q in range(P):  # the gradient's slice [lo, hi), as the full tensor holds it
-                buf[q][:hi - lo].copy_(grads[q][lo:hi])
-            ready[b].record(producer)
-        stepper.wait_event(ready[b])
-        sa, sk = zdp.make_step_args([x[:hi - lo] for x in buf], st[0], st[1], st[2], reps, n=n,
-                                    scale=wl.scale, t=wl.t0, off=lo, length=hi - lo,
-                                    d_overflow=words[0:4].view(torch.int32), **HP)
-        keep_all.append((sa, sk))
-        zdp.zdp_step(sa, stepper)
-        done[b].record(stepper)
+    # streamed: the producer copies each bucket's slice of the resident gradients
+    st, reps, words = state()
+    ss = streaming.StreamedStep(P, n, bucket, st[0], st[1], st[2], reps, scale=wl.scale,
+                                d_overflow=words[0:4].view(torch.int32),
+                                d_sumsq=words[8:16].view(torch.float64), buffers=nbuf, **HP)
+
+    def produce(views, lo, hi):
+        for q in range(P):
+            views[q].copy_(grads[q][lo:hi])
+
+    ss.run(wl.t0, produce)
     torch.cuda.synchronize()
-    assert len(bounds) > 2
+    assert len(ss.bounds) > nbuf
     for x, y, name in zip(st, st_ref, ("master", "m", "v")):
         assert_bits_equal(x[:n].cpu().numpy(), y[:n].cpu().numpy(), f"streamed {name}")
     for q in range(P):
         assert np.array_equal(bits_of(reps[q]), bits_of(reps_ref[q])), f"replica {q}"
     assert int(words[0:4].view(torch.int32).item()) == int(words_ref[0:4].view(torch.int32).item())
+    s_ref = float(words_ref[8:16].view(torch.float64).item())
+    assert abs(float(words[8:16].view(torch.float64).item()) - s_ref) <= 1e-9 * s_ref
