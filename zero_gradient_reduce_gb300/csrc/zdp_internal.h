@@ -59,6 +59,22 @@ inline bool fused_sqv(int P, int mt) {
   return P == 1 || P == 4 || P == 8 || P == 40 || P == 48 || P == 56 || P == 64;
 }
 
+// The bf16-moment fused step at P = 1 and 2 runs k_fused_mt<P, GT,
+// ZDP_MOMENTS_BF16, SQV, MINB>: whether it tests the squares' range per
+// vector, and the resident blocks per SM its register allocation must allow.
+#ifndef ZDP_BF16M_P1_SQV
+#define ZDP_BF16M_P1_SQV true
+#endif
+#ifndef ZDP_BF16M_P1_MINB
+#define ZDP_BF16M_P1_MINB 8
+#endif
+#ifndef ZDP_BF16M_P2_SQV
+#define ZDP_BF16M_P2_SQV true
+#endif
+#ifndef ZDP_BF16M_P2_MINB
+#define ZDP_BF16M_P2_MINB 8
+#endif
+
 // Blocks per SM of the reduce-scatter for P ranks; measured fractions of the
 // copy ceiling at the chosen caps: P = 2: 8 blocks, 0.95; P = 4: 16, 0.99
 // (12: 0.96); P = 8, 16, 64: 12, 0.98-0.99.

@@ -532,6 +532,51 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
   wait_previous_launch();
 }
 
+// The fused step for exactly P <= 8 ranks with the moment type MT fixed at
+// compile time, and MINB resident blocks per SM asked of the register
+// allocator (__launch_bounds__).  The operations and their order are those
+// of k_fused.  It serves the bf16-moment step at P = 1 and 2: there k_fused,
+// which carries the code of both moment types, is bound by instruction issue
+// and latency at 8 resident blocks (0.78 and 0.84 of the copy ceiling on
+// GB300), and this kernel's register allocation runs 0.89 and 0.92.
+template <int P, int GT, int MT, bool SQV, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) k_fused_mt(const __grid_constant__ KParams p) {
+  allow_next_launch();
+  const bool sq = p.sumsq != nullptr;
+  bool bad = false;
+  SumSq ss;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const int64_t vlo = p.lo / kVec, vhi = (p.hi + kVec - 1) / kVec;
+  for (int64_t vi = vlo + tid; vi < vhi; vi += stride) {
+    const int64_t i0 = vi * kVec;
+    const int r = owner_of(i0, p, P);
+    if (i0 >= p.lo && i0 + kVec <= p.hi && i0 + kVec <= static_cast<int64_t>(r + 1) * p.S) {
+      float w[kVec], m[kVec], v[kVec], g[kVec];
+      ld_f8(p.w + i0, w);
+      ld_moments8(p.m, p.v, MT, i0, m, v);
+      ring_sum_vec<P, true, GT>(p, P, r, i0, g);
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) g[k] = __fmul_rn(g[k], p.scale);
+      account<SQV>(g, sq, bad, ss);
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) adamw(w[k], m[k], v[k], g[k], p.ad);
+      st_f8(p.w + i0, w);
+      st_moments8(p.m, p.v, MT, i0, m, v);
+      const uint4 b = pack_bf16x8(w);
+#pragma unroll
+      for (int q = 0; q < P; ++q) st16(p.rep[q] + i0, b);
+    } else {
+      for (int k = 0; k < kVec; ++k) {
+        const int64_t i = i0 + k;
+        if (i >= p.lo && i < p.hi) fused_elem<GT>(p, P, i, sq, bad, ss);
+      }
+    }
+  }
+  publish(p, bad, ss);
+  wait_previous_launch();
+}
+
 // Reduce-scatter only: reduced gradients to gout.
 template <int PT, bool EXACT, int GT, bool VEC>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ KParams p) {
