@@ -68,6 +68,11 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=1 << 24,
                     help="parameters per oracle step in the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-whole", action="store_true",
+                    help="with --impl reference: time the oracle on whole units of the workload "
+                         "instead of a bounded sample per step: one step over the whole model, "
+                         "or for a streamed model its first, last and shard-straddling buckets "
+                         "(minutes of CPU time and tens of GB of host memory)")
     ap.add_argument("--zpp", action="store_true",
                     help="the ZeRO++ step (int8 block-quantized gradients in, int8 replicas out) "
                          "on the workload instead of zdp_step")
@@ -412,6 +417,36 @@ def run_ours(args):
     ms_per_step = elapsed_ms / K
     value = whole_job_rate(n, K, world, elapsed_ms)
 
+    # ---- latency floor of a step this small (timed alone after an L2 flush):
+    # a minimal launch (16-byte zdp_copy) and a cold zdp_copy that moves the
+    # step's own algorithmic bytes (half read, half written)
+    floor = None
+    if flush is not None and rank == 0:
+        def cold_us(fn, reps=20):
+            out = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                out.append(e0.elapsed_time(e1) * 1e3)
+            return sorted(out)[len(out) // 2]
+        half = (bytes_per_param(P, args.moments) * n // 2 + 15) // 16 * 16
+        src = torch.empty(half, dtype=torch.uint8, device=dev)
+        dst = torch.empty(half, dtype=torch.uint8, device=dev)
+        launch_us = cold_us(lambda: zdp.zdp_copy(dst, src, 16, stream))
+        copy_us = cold_us(lambda: zdp.zdp_copy(dst, src, half, stream))
+        peak_gbs = measured_peak()[0]
+        floor = {"min_launch_us": launch_us, "step_bytes_copy_us": copy_us,
+                 "step_bytes_at_peak_us": 2 * half / (peak_gbs * 1e3),
+                 "step_us": kernel_ms_median * 1e3,
+                 "step_over_copy": kernel_ms_median * 1e3 / copy_us,
+                 "how": ("medians of 20, each after an L2 flush: a 16-byte zdp_copy (one "
+                         "launch), and zdp_copy of the step's algorithmic bytes")}
+        del src, dst
+
     # ---- end to end through the C ABI: gradients from pinned host memory
     e2e = None
     if not args.no_e2e and not args.check_overflow:
@@ -476,6 +511,8 @@ def run_ours(args):
         }
         if e2e is not None:
             out["e2e"] = e2e
+        if floor is not None:
+            out["latency_floor"] = floor
         if args.check_overflow:
             out["metric_note"] = ("the overflow-checked step; the two-pass form moves 8 more "
                                   "bytes per parameter than the algorithmic bytes above")
@@ -788,6 +825,73 @@ def run_reference(args):
                          "host_cores": os.cpu_count(), "sample": sample},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_oracle_whole(args):
+    """The CPU oracle on whole units of the workload, one host core: for a
+    resident model one step over every parameter, for a streamed model
+    whole buckets (the first, the last, and each one that holds a shard
+    boundary), each step timed alone.  One JSON line per unit and a summary
+    line.  Inputs: the workload's seeded gradients; for buckets, master/m/v
+    of the workload's distributions drawn per bucket (the oracle's time does
+    not depend on their values)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from zero_gradient_reduce_gb300 import workloads
+
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    oracle.build()
+    wl = workloads.by_name(args.workload)
+    P, n = wl.P, wl.n
+    S = -(-n // P)
+    if wl.streamed:
+        B = wl.bucket_elems
+        bounds = [(lo, min(n, lo + B)) for lo in range(0, n, B)]
+        keep = {0, len(bounds) - 1}
+        keep |= {k for k, (lo, hi) in enumerate(bounds) if any(lo < r * S < hi for r in range(1, P))}
+        units = [bounds[k] for k in sorted(keep)]
+    else:
+        units = [(0, n)]
+    total_params, total_s = 0, 0.0
+    for lo, hi in units:
+        length = hi - lo
+        g = np.empty((P, length), np.uint16)
+        for q in range(P):
+            t = workloads.fill_grads(torch.empty(length, dtype=torch.bfloat16), wl, q, 0,
+                                     args.seed, lo)
+            g[q] = t.view(torch.int16).numpy().view(np.uint16)
+            del t
+        rng = np.random.default_rng(workloads.key(args.seed, workloads.STREAM_MASTER, 0, 0, lo))
+        w = (rng.standard_normal(length, dtype=np.float32) * np.float32(0.02))
+        if wl.fresh_state:
+            m = np.zeros(length, np.float32)
+            v = np.zeros(length, np.float32)
+        else:
+            m = rng.standard_normal(length, dtype=np.float32) * np.float32(1e-4)
+            v = rng.uniform(0.0, 1e-6, length).astype(np.float32)
+        rep = np.empty((P, length), np.uint16)
+        t0 = time.perf_counter()
+        oracle.step(g, oracle.BF16, w, m, v, rep, n, lo, length, wl.scale, t=wl.t0, base=lo,
+                    **HP)
+        el = time.perf_counter() - t0
+        total_params += length
+        total_s += el
+        print(json.dumps({"impl": "reference", "kind": "oracle", "workload": wl.name,
+                          "unit": [lo, hi], "params": length, "seconds": el,
+                          "params_per_s": length / el, "cores": 1}), flush=True)
+        del g, w, m, v, rep
+    print(json.dumps({
+        "impl": "reference", "kind": "oracle", "workload": wl.name, "n_params": n, "P": P,
+        "units": len(units), "params_timed": total_params, "seconds": total_s,
+        "params_per_s": total_params / total_s, "cores": 1, "host_cores": os.cpu_count(),
+        "full_step_seconds": n / (total_params / total_s),
+        "what": ("one oracle step over the whole model" if not wl.streamed else
+                 "whole buckets: the first, the last and each shard-straddling one"),
     }), flush=True)
 
 
@@ -1244,7 +1348,9 @@ def run_overlap(args):
 
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.impl == "reference" and args.oracle_whole:
+        run_oracle_whole(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.zpp:
         run_zpp(args)
