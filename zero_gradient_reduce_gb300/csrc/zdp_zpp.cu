@@ -73,9 +73,35 @@ __device__ __forceinline__ int quant_rcp(float x, float scale, float rcp) {
 }
 
 // Codes of 8 values sharing one block scale (0 for an all-zero block).
+// With a normal, finite scale (the usual case) every |x| <= 127 * scale is
+// finite and rcp = fl(1/scale) is within 2^-24 of 1/scale, so
+// |y| = |fl(x * rcp)| < 127 * (1 + 2^-22) < 127.5 and the rounded code needs
+// no clamp; the 8 codes take the multiply path with one test for all of
+// them (none of the 8 within 1e-4 of a half-integer), the same test as
+// quant_rcp's per element.  ONE_TEST = false keeps the per-element form
+// (quant_rcp) throughout: the kernels of 16 or more ranks spill registers
+// with the other.
+template <bool ONE_TEST = true>
 __device__ __forceinline__ void quant8(const float (&x)[kVec], float scale, int (&q)[kVec]) {
   const float rcp = __frcp_rn(scale);
-  if (scale == 0.0f) {
+  if (ONE_TEST && scale >= 0x1p-126f && scale <= 3.40282347e38f) {
+    float t[kVec];
+    bool near_tie = false;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      const float y = __fmul_rn(x[e], rcp);
+      t[e] = __fadd_rn(y, 12582912.0f);
+      const float d = __fsub_rn(y, __fsub_rn(t[e], 12582912.0f));  // exact: |d| <= 0.5
+      near_tie |= !(fabsf(d) < 0.4999f);
+    }
+    if (!near_tie) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) q[e] = __float_as_int(t[e]) - 0x4B400000;
+      return;
+    }
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) q[e] = quant_rcp(x[e], scale, rcp);
+  } else if (scale == 0.0f) {
 #pragma unroll
     for (int e = 0; e < kVec; ++e) q[e] = 0;
   } else if (isfinite(rcp)) {
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : Z
     for (int e = 0; e < kVec; ++e) abits = max(abits, abs_bits(pv[e]));
     const float sc = __fdiv_rn(warp_absmax(abits), 127.0f);
     int qv[kVec];
-    quant8(pv, sc, qv);
+    quant8<(PT <= 8)>(pv, sc, qv);
     if (cnt == kVec) {
       const uint2 packed = pack_i8x8(qv);
       for (int q = 0; q < P; ++q) st8(p.rq[q] + i0, packed);
