@@ -156,6 +156,14 @@ def step_flushes_l2(wl, moments="f32", l2=GB300_L2_BYTES):
     return bytes_per_param(wl.P, moments) * wl.n < 4 * l2
 
 
+def fused_kernel_name(P: int, moments: str) -> str:
+    """The kernel the fused step launches for P ranks and the moment type on
+    the 16-byte path (the choice the library's fused-step launcher makes)."""
+    fixed = {("f32", 1), ("f32", 4), ("f32", 6), ("f32", 8), ("bf16", 1), ("bf16", 2)}
+    name = "k_fused_mt" if (moments, P) in fixed else "k_fused"
+    return f"{name}<P={P}, bf16 gradients, {moments} moments>"
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -493,7 +501,7 @@ def run_ours(args):
                 "frac": achieved / peak,
                 "traffic": traffic,
                 "peak_source": f"{peak_kind} HBM copy bandwidth",
-                "kernel": (f"k_fused<P={P}, bf16>" if not args.check_overflow else
+                "kernel": (fused_kernel_name(P, args.moments) if not args.check_overflow else
                            "k_step_coop (one launch) or k_reduce + k_adam_gather (two passes)"),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "kernel_ms": kernel_ms,

@@ -54,26 +54,12 @@ inline int fused_cap(int P, int mt) {
 // 1.001, 7: 0.994, 8: 1.009, 12: 0.988, 16: 0.987, 24: 0.996, 32: 1.000, 40:
 // 1.011, 48: 1.007, 56: 1.006, 64: 1.005; bf16 moments: P = 2: 1.009, 4:
 // 0.988, 8: 0.989, 64: 1.004.  Chosen where the gain is at least 0.5 %.
+// (Of these, P = 1, 4 and 8 with fp32 moments and P = 2 with bf16 moments now
+// run k_fused_mt, which tests per vector; see pick_fused_mt.)
 inline bool fused_sqv(int P, int mt) {
   if (mt != ZDP_MOMENTS_F32) return P == 2;
   return P == 1 || P == 4 || P == 8 || P == 40 || P == 48 || P == 56 || P == 64;
 }
-
-// The bf16-moment fused step at P = 1 and 2 runs k_fused_mt<P, GT,
-// ZDP_MOMENTS_BF16, SQV, MINB>: whether it tests the squares' range per
-// vector, and the resident blocks per SM its register allocation must allow.
-#ifndef ZDP_BF16M_P1_SQV
-#define ZDP_BF16M_P1_SQV true
-#endif
-#ifndef ZDP_BF16M_P1_MINB
-#define ZDP_BF16M_P1_MINB 8
-#endif
-#ifndef ZDP_BF16M_P2_SQV
-#define ZDP_BF16M_P2_SQV true
-#endif
-#ifndef ZDP_BF16M_P2_MINB
-#define ZDP_BF16M_P2_MINB 8
-#endif
 
 // Blocks per SM of the reduce-scatter for P ranks; measured fractions of the
 // copy ceiling at the chosen caps: P = 2: 8 blocks, 0.95; P = 4: 16, 0.99
