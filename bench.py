@@ -211,11 +211,20 @@ def copy_ceiling_gbs(dev, reps=10):
     return out
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and blank lines, each line stripped."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", line).strip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash() -> str:
+    """sha256 prefix of the fused kernel's source files, comments excluded (a
+    comment edit leaves the compiled kernel, and so its counters, as they were)."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

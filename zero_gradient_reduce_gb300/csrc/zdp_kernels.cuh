@@ -535,10 +535,11 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ KPar
 // The fused step for exactly P <= 8 ranks with the moment type MT fixed at
 // compile time, and MINB resident blocks per SM asked of the register
 // allocator (__launch_bounds__).  The operations and their order are those
-// of k_fused.  It serves the bf16-moment step at P = 1 and 2: there k_fused,
-// which carries the code of both moment types, is bound by instruction issue
-// and latency at 8 resident blocks (0.78 and 0.84 of the copy ceiling on
-// GB300), and this kernel's register allocation runs 0.89 and 0.92.
+// of k_fused, which carries the code of both moment types.  It runs where it
+// measured faster (pick_fused_mt in kernels_grad.inc), most of all for bf16
+// moments at P = 1 and 2: there k_fused is bound by instruction issue and
+// latency (0.78 and 0.84 of the copy ceiling on GB300) and this kernel at 8
+// blocks per SM runs 0.93 and 0.94.
 template <int P, int GT, int MT, bool SQV, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) k_fused_mt(const __grid_constant__ KParams p) {
   allow_next_launch();
