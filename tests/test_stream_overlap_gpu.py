@@ -99,3 +99,43 @@ def test_streamed_buckets_on_two_streams_equal_one_call(P, n, bucket, nbuf):
     assert int(words[0:4].view(torch.int32).item()) == int(words_ref[0:4].view(torch.int32).item())
     s_ref = float(words_ref[8:16].view(torch.float64).item())
     assert abs(float(words[8:16].view(torch.float64).item()) - s_ref) <= 1e-9 * s_ref
+
+
+def test_streamed_fp16_gradients_and_bf16_moments_equal_one_call():
+    # the driver's other storage types: fp16 gradients (loss-scaled) and the
+    # 12-byte state (bf16 m and v), three bucket buffers
+    P, n, bucket = 4, 5_000_011, 700_001
+    wl = workloads.Workload(f"flat_{n}_p{P}_fp16", P=P, n=n, tensors=workloads._flat(n),
+                            grad_dtype="fp16", fp16_loss_scale=2.0 ** 16, t0=5)
+    seed = 13
+    S = -(-n // P)
+    grads = [workloads.fill_grads(torch.empty(n, dtype=torch.float16, device="cuda"), wl, q,
+                                  0, seed) for q in range(P)]
+
+    def state():
+        st = torch.empty(3, P * S, dtype=torch.float32, device="cuda")
+        workloads.fill_state(st[0], st[1], st[2], wl, seed)
+        mv = st[1:].to(torch.bfloat16)
+        reps = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        return st[0].clone(), mv[0], mv[1], reps, torch.zeros(16, dtype=torch.uint8, device="cuda")
+
+    w0, m0, v0, r0, k0 = state()
+    a, keep = zdp.make_step_args(grads, w0, m0, v0, r0, n=n, scale=wl.scale, t=wl.t0,
+                                 d_overflow=k0[0:4].view(torch.int32), moments="bf16", **HP)
+    zdp.zdp_step(a)
+    w1, m1, v1, r1, k1 = state()
+    ss = streaming.StreamedStep(P, n, bucket, w1, m1, v1, r1, scale=wl.scale,
+                                grad_dtype=torch.float16, moments="bf16",
+                                d_overflow=k1[0:4].view(torch.int32), buffers=3, **HP)
+
+    def produce(views, lo, hi):
+        for q in range(P):
+            views[q].copy_(grads[q][lo:hi])
+
+    ss.run(wl.t0, produce)
+    torch.cuda.synchronize()
+    assert_bits_equal(w1[:n].cpu().numpy(), w0[:n].cpu().numpy(), "streamed master")
+    assert np.array_equal(bits_of(m1[:n]), bits_of(m0[:n])) and np.array_equal(bits_of(v1[:n]), bits_of(v0[:n]))
+    for q in range(P):
+        assert np.array_equal(bits_of(r1[q]), bits_of(r0[q])), f"replica {q}"
+    assert int(k1[0:4].view(torch.int32).item()) == int(k0[0:4].view(torch.int32).item()) == 0

@@ -40,17 +40,18 @@ struct DriverEntryPoints {
 const DriverEntryPoints& driver_entry_points() {
   static const DriverEntryPoints eps = [] {
     DriverEntryPoints d;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess && q == cudaDriverEntryPointSuccess)
-      d.get_current = reinterpret_cast<CtxGetCurrentFn>(f);
-    f = nullptr;
-    q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess && q == cudaDriverEntryPointSuccess)
-      d.get_id = reinterpret_cast<CtxGetIdFn>(f);
-    cudaGetLastError();  // a failed query leaves nothing sticky behind
+    auto query = [](const char* name) -> void* {
+      void* f = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      const cudaError_t e = cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess) {
+        cudaGetLastError();  // clear this query's own (non-sticky) error, nothing older
+        return nullptr;
+      }
+      return q == cudaDriverEntryPointSuccess ? f : nullptr;
+    };
+    d.get_current = reinterpret_cast<CtxGetCurrentFn>(query("cuCtxGetCurrent"));
+    d.get_id = reinterpret_cast<CtxGetIdFn>(query("cuCtxGetId"));
     return d;
   }();
   return eps;
