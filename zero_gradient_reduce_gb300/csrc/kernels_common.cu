@@ -95,6 +95,9 @@ cudaError_t launch_reduce(const KParams& p, int gdt, bool vec, int num_sms, cuda
 
 cudaError_t launch_adam_gather(const KParams& p, bool vec, int num_sms, cudaStream_t s,
                                bool overlap_prev) {
+  if (vec && p.nrep == 8 && p.mt == ZDP_MOMENTS_F32)
+    return launch_fn(reinterpret_cast<const void*>(&k_adam_gather_mt<8, ZDP_MOMENTS_F32>), p, vec,
+                     num_sms, adam_gather_cap(p.nrep, p.mt), s, overlap_prev);
   const void* fn = vec ? reinterpret_cast<const void*>(&k_adam_gather<true>)
                        : reinterpret_cast<const void*>(&k_adam_gather<false>);
   const int cap = p.nrep == 0 ? ZDP_CAP_ADAM : adam_gather_cap(p.nrep, p.mt);
