@@ -158,7 +158,7 @@ def step_flushes_l2(wl, moments="f32", l2=GB300_L2_BYTES):
 
 def fused_kernel_name(P: int, moments: str) -> str:
     """The kernel the fused step launches for P ranks and the moment type on
-    the 16-byte path (the choice the library's fused-step launcher makes)."""
+    the 16-byte path: the table of pick_fused_mt in csrc/kernels_grad.inc."""
     fixed = {("f32", 1), ("f32", 4), ("f32", 6), ("f32", 8), ("bf16", 1), ("bf16", 2)}
     name = "k_fused_mt" if (moments, P) in fixed else "k_fused"
     return f"{name}<P={P}, bf16 gradients, {moments} moments>"
