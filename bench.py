@@ -1114,6 +1114,9 @@ def run_zpp(args):
     stream = torch.cuda.current_stream(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.warmup + args.steps)]
+    sampler = ClockSampler(gpu_id_for_smi(dev.index or 0))
+    sampler.start()
+    wall0 = time.time()
     for k, (e0, e1) in enumerate(ev):
         a.t = k + 1
         words.zero_()
@@ -1121,6 +1124,8 @@ def run_zpp(args):
         zdp.zdp_step_zpp(a, stream)
         e1.record(stream)
     torch.cuda.synchronize()
+    wall1 = time.time()
+    sampler.stop()
     ms = sum(e0.elapsed_time(e1) for e0, e1 in ev[args.warmup:]) / args.steps
     state_b = 24 if args.moments == "f32" else 16
     bpp = 2 * P + state_b + 8 * P / zdp.ZDP_QBLOCK
@@ -1131,13 +1136,17 @@ def run_zpp(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded bf16 gradients block-quantized to int8",
-        "config": dict(config_of(wl), moments=args.moments, zpp="int8 blocks of 256, both ways"),
+        "config": dict(config_of(wl, moments=args.moments),
+                       state=("fp32 master/m/v" if args.moments == "f32" else
+                              "fp32 master, bf16 m/v") + ", int8 replicas with block scales",
+                       zpp="int8 blocks of 256, both ways"),
         "hbm_tbs": achieved / 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_param": bpp},
         "gpu_launches": args.steps,
+        "clocks": sampler.summary(wall0, wall1),
         "metric_note": "ZeRO++ variant of the step (quantized communication), not the headline",
     }), flush=True)
 

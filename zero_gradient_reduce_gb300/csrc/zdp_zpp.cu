@@ -234,10 +234,14 @@ __device__ __forceinline__ void publish_to(int32_t* flag, double* sumsq, bool ba
   publish_to(flag, sumsq, bad, whole);
 }
 
-template <int PT, bool F64SQ>
-__global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : ZDP_ZPP_MIN_BLOCKS)
-    k_zpp(const __grid_constant__ ZppParams p) {
+// MT: the moment type when fixed at compile time (the bf16-moment kernels), or
+// -1 to follow p.mt; MINB: the resident blocks per SM the register allocation
+// must allow.
+template <int PT, bool F64SQ, int MT = -1,
+          int MINB = (PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : ZDP_ZPP_MIN_BLOCKS)>
+__global__ void __launch_bounds__(kThreads, MINB) k_zpp(const __grid_constant__ ZppParams p) {
   const int P = PT > 0 ? PT : p.P;
+  const int mt = MT >= 0 ? MT : p.mt;
   const bool sq = p.sumsq != nullptr;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : Z
       if (full) {
         float w[kVec], m[kVec], v[kVec];
         ld_f8(p.w + i0, w);
-        ld_moments8(p.m, p.v, p.mt, i0, m, v);
+        ld_moments8(p.m, p.v, mt, i0, m, v);
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
           g[e] = __fmul_rn(g[e], p.scale);
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : Z
         vec_set<ZDP_BF16>(pv, pack_bf16x8(w));  // the bf16 parameters, widened
         account(g, sq, bad, ss);
         st_f8(p.w + i0, w);
-        st_moments8(p.m, p.v, p.mt, i0, m, v);
+        st_moments8(p.m, p.v, mt, i0, m, v);
       } else {
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
@@ -294,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, PT > 8 ? ZDP_ZPP_MIN_BLOCKS_WIDE : Z
             const int64_t i = i0 + e;
             const float ge = __fmul_rn(g[e], p.scale);
             account1(ge, sq, bad, ss);
-            float w = p.w[i], m = ld_moment(p.m, i, p.mt), v = ld_moment(p.v, i, p.mt);
+            float w = p.w[i], m = ld_moment(p.m, i, mt), v = ld_moment(p.v, i, mt);
             adamw(w, m, v, ge, p.ad);
             p.w[i] = w;
-            st_moment(p.m, i, p.mt, m);
-            st_moment(p.v, i, p.mt, v);
+            st_moment(p.m, i, mt, m);
+            st_moment(p.v, i, mt, v);
             pv[e] = widen1<ZDP_BF16>(to_bf16(w));
           }
         }
@@ -410,6 +414,38 @@ bool zpp_f64_sumsq(int P, int mt) {
   return true;
 }
 
+// The bf16-moment kernels with the moment type fixed at compile time, for the
+// P (and sum-of-squares form) where they measured faster on GB300 than the
+// kernel that reads the moment type at run time; nullptr elsewhere.  The
+// resident blocks per SM asked of the register allocator are the measured
+// best.  Fraction of the copy ceiling, flat n = 2^28, run-time -> fixed
+// moment type: P = 1: 0.594 -> 0.603 (7 blocks); 2: 0.570 -> 0.593 (6);
+// 3: 0.647 -> 0.684 (8); 4: 0.685 -> 0.754 (8); 5: 0.716 -> 0.753 (8);
+// 6: 0.745 -> 0.804 (6); 7: 0.790 -> 0.846 (8); 8: 0.795 -> 0.852 (7);
+// 12, the generic kernel: 0.710 -> 0.733 (8); 16: 0.719 -> 0.725 (6);
+// 64: 0.808 -> 0.816 (6); 32 stays with the run-time kernel (0.806 against
+// 0.790).  With the sum of squares in the other form than the one measured,
+// the run-time kernel serves.
+const void* zpp_kernel_bf16m(int P, bool f64) {
+  constexpr int B = ZDP_MOMENTS_BF16;
+  auto k = [](auto kernel) { return reinterpret_cast<const void*>(kernel); };
+  if (f64 != zpp_f64_sumsq(P, B)) return nullptr;
+  switch (P) {
+    case 1: return k(&k_zpp<1, true, B, 7>);
+    case 2: return k(&k_zpp<2, true, B, 6>);
+    case 3: return k(&k_zpp<3, true, B, 8>);
+    case 4: return k(&k_zpp<4, true, B, 8>);
+    case 5: return k(&k_zpp<5, true, B, 8>);
+    case 6: return k(&k_zpp<6, true, B, 6>);
+    case 7: return k(&k_zpp<7, true, B, 8>);
+    case 8: return k(&k_zpp<8, true, B, 7>);
+    case 16: return k(&k_zpp<16, false, B, 6>);
+    case 32: return nullptr;
+    case 64: return k(&k_zpp<64, false, B, 6>);
+    default: return k(&k_zpp<0, true, B, 8>);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cudaStream_t s) {
@@ -440,8 +476,8 @@ cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cuda
   const int64_t blocks = (a->len + kQB - 1) / kQB;
   if (blocks == 0) return cudaSuccess;
   const bool f64 = p.sumsq != nullptr && zpp_f64_sumsq(P, p.mt);
-  const void* fn;
-  switch (P) {
+  const void* fn = p.mt == ZDP_MOMENTS_BF16 ? zpp_kernel_bf16m(P, f64) : nullptr;
+  if (!fn) switch (P) {
     case 1: fn = zpp_kernel<1>(f64); break;
     case 2: fn = zpp_kernel<2>(f64); break;
     case 3: fn = zpp_kernel<3>(f64); break;
