@@ -414,22 +414,38 @@ bool zpp_f64_sumsq(int P, int mt) {
   return true;
 }
 
-// The bf16-moment kernels with the moment type fixed at compile time, for the
-// P (and sum-of-squares form) where they measured faster on GB300 than the
+// The kernels with the moment type fixed at compile time, for the P, moment
+// type (and sum-of-squares form) where they measured faster on GB300 than the
 // kernel that reads the moment type at run time; nullptr elsewhere.  The
 // resident blocks per SM asked of the register allocator are the measured
 // best.  Fraction of the copy ceiling, flat n = 2^28, run-time -> fixed
-// moment type: P = 1: 0.594 -> 0.603 (7 blocks); 2: 0.570 -> 0.593 (6);
-// 3: 0.647 -> 0.684 (8); 4: 0.685 -> 0.754 (8); 5: 0.716 -> 0.753 (8);
-// 6: 0.745 -> 0.804 (6); 7: 0.790 -> 0.846 (8); 8: 0.795 -> 0.852 (7);
-// 12, the generic kernel: 0.710 -> 0.733 (8); 16: 0.719 -> 0.725 (6);
-// 64: 0.808 -> 0.816 (6); 32 stays with the run-time kernel (0.806 against
-// 0.790).  With the sum of squares in the other form than the one measured,
-// the run-time kernel serves.
-const void* zpp_kernel_bf16m(int P, bool f64) {
-  constexpr int B = ZDP_MOMENTS_BF16;
+// moment type (blocks per SM):
+//   bf16 moments: P = 1: 0.594 -> 0.603 (7); 2: 0.570 -> 0.593 (6); 3: 0.647
+//   -> 0.684 (8); 4: 0.685 -> 0.754 (8); 5: 0.716 -> 0.753 (8); 6: 0.745 ->
+//   0.804 (6); 7: 0.790 -> 0.846 (8); 8: 0.795 -> 0.852 (7); 12, the generic
+//   kernel: 0.710 -> 0.733 (8); 16: 0.719 -> 0.725 (6); 64: 0.808 -> 0.816
+//   (6); P = 32 keeps the run-time kernel (0.806 against 0.790).
+//   fp32 moments: P = 1: 0.846 -> 0.862 (7); 2: 0.775 -> 0.799 (6); 3: 0.834
+//   -> 0.885 (8); 4: 0.895 -> 0.910 (8); 5: 0.908 -> 0.918 (6); 6: 0.918 ->
+//   0.943 (8); P = 7, 8 and above keep the run-time kernel (P = 8: 0.873
+//   against 0.864 at 8 blocks).
+// With the sum of squares in the other form than the one measured, the
+// run-time kernel serves.
+const void* zpp_kernel_fixed(int P, int mt, bool f64) {
+  constexpr int B = ZDP_MOMENTS_BF16, F = ZDP_MOMENTS_F32;
   auto k = [](auto kernel) { return reinterpret_cast<const void*>(kernel); };
-  if (f64 != zpp_f64_sumsq(P, B)) return nullptr;
+  if (f64 != zpp_f64_sumsq(P, mt)) return nullptr;
+  if (mt == F) {
+    switch (P) {
+      case 1: return k(&k_zpp<1, true, F, 7>);
+      case 2: return k(&k_zpp<2, true, F, 6>);
+      case 3: return k(&k_zpp<3, true, F, 8>);
+      case 4: return k(&k_zpp<4, true, F, 8>);
+      case 5: return k(&k_zpp<5, true, F, 6>);
+      case 6: return k(&k_zpp<6, true, F, 8>);
+      default: return nullptr;
+    }
+  }
   switch (P) {
     case 1: return k(&k_zpp<1, true, B, 7>);
     case 2: return k(&k_zpp<2, true, B, 6>);
@@ -476,7 +492,7 @@ cudaError_t launch_zpp(const zdp_zpp_args* a, const AdamK& ad, int num_sms, cuda
   const int64_t blocks = (a->len + kQB - 1) / kQB;
   if (blocks == 0) return cudaSuccess;
   const bool f64 = p.sumsq != nullptr && zpp_f64_sumsq(P, p.mt);
-  const void* fn = p.mt == ZDP_MOMENTS_BF16 ? zpp_kernel_bf16m(P, f64) : nullptr;
+  const void* fn = zpp_kernel_fixed(P, p.mt, f64);
   if (!fn) switch (P) {
     case 1: fn = zpp_kernel<1>(f64); break;
     case 2: fn = zpp_kernel<2>(f64); break;
