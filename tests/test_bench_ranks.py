@@ -95,3 +95,45 @@ def test_headline_profile_matches_the_kernel_sources():
     assert traffic is not None, "kernel sources changed since profiles/ was captured"
     alg = 56 * 1_311_227_904
     assert 0.99 * alg < traffic < 1.01 * alg
+
+
+def test_kernel_label_follows_the_fused_dispatch_table():
+    # The benchmark line names the fused kernel from its own copy of the
+    # table in pick_fused_mt (csrc/kernels_grad.inc); the two must agree.
+    import re
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    src = open(os.path.join(ROOT, "zero_gradient_reduce_gb300", "csrc", "kernels_grad.inc")).read()
+    body = src[src.index("const void* pick_fused_mt(int P, int mt) {"):]
+    body = body[:body.index("\n}\n")]
+    table = set()
+    for P, mt in re.findall(r"case (\d+): return reinterpret_cast<const void\*>\(&k_fused_mt<\d+, ZDP_GT, ZDP_MOMENTS_(F32|BF16)", body):
+        table.add(("f32" if mt == "F32" else "bf16", int(P)))
+    assert table, "no k_fused_mt cases found"
+    for moments in ("f32", "bf16"):
+        for P in range(1, 65):
+            named = bench.fused_kernel_name(P, moments).startswith("k_fused_mt<")
+            assert named == ((moments, P) in table), (moments, P)
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    code = "int f(int x) {  // doubles\n  return 2 * x; /* two\n lines */\n}\n"
+    assert bench._code_only(code) == bench._code_only(
+        "int f(int x) {\n\n  return 2 * x;   // another note\n}\n")
+    assert bench._code_only(code) != bench._code_only(code.replace("2 * x", "3 * x"))
+
+
+def test_flat_slice_workloads_by_name():
+    from zero_gradient_reduce_gb300 import workloads
+
+    for P in (1, 2, 8, 64):
+        wl = workloads.by_name(f"flat_p{P}_32m")
+        assert wl.P == P and wl.n == 32 * 2**20 and wl.fresh_state
+    assert workloads.by_name("flat_p8_32m").name == workloads.flat_p8_32m().name
+    with pytest.raises(KeyError):
+        workloads.by_name("flat_px_32m")
