@@ -121,6 +121,17 @@ def whole_job_rate(units_per_rank: int, steps: int, world: int, slowest_ms: floa
     return world * units_per_rank * steps / (slowest_ms / 1e3)
 
 
+def state_rows(length: int, device):
+    """fp32 master, m and v of `length` elements as rows of one allocation,
+    each row starting on a 256-byte boundary whatever P * S is (the vector
+    paths want 16-byte-aligned state).  Returns (buffer, master, m, v)."""
+    import torch
+
+    row = -(-length // 64) * 64
+    buf = torch.empty(3, row, dtype=torch.float32, device=device)
+    return buf, buf[0, :length], buf[1, :length], buf[2, :length]
+
+
 def bytes_per_param(P: int, moments: str = "f32") -> int:
     # P bf16 gradient reads + master/m/v read and written + P bf16 replica writes
     state = 12 if moments == "f32" else 8
@@ -353,14 +364,15 @@ def run_ours(args):
     grads = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
     for q in range(P):
         workloads.fill_grads(grads[q], wl, q, 0, seed)
-    state = torch.empty(3, n_pad, dtype=torch.float32, device=dev)
-    master, m, v = state[0], state[1], state[2]
+    state, master, m, v = state_rows(n_pad, dev)
     workloads.fill_state(master, m, v, wl, seed)
     if args.moments == "bf16":  # the same moments, held in bf16
-        mv16 = state[1:].to(torch.bfloat16)
-        m, v = mv16[0], mv16[1]
-        state = state[:1].clone()
-        master = state[0]
+        # One allocation each: packed into one (2, P*S) buffer, v would start
+        # 2*P*S bytes in, off the 16-byte boundary the vector path needs
+        # whenever P*S is not a multiple of 8.
+        m, v = m.to(torch.bfloat16), v.to(torch.bfloat16)
+        master = master.clone()
+        state = None
     replicas = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
     words = torch.zeros(16, dtype=torch.uint8, device=dev)
     flag = words[0:4].view(torch.int32)
@@ -1098,16 +1110,14 @@ def run_zpp(args):
         del g
         gq.append(qq)
         gs.append(sc)
-    st = torch.empty(3, P * S, dtype=torch.float32, device=dev)
-    workloads.fill_state(st[0], st[1], st[2], wl, args.seed)
-    m, v = st[1], st[2]
-    if args.moments == "bf16":
-        mv16 = st[1:].to(torch.bfloat16)
-        m, v = mv16[0], mv16[1]
+    st, w, m, v = state_rows(P * S, dev)
+    workloads.fill_state(w, m, v, wl, args.seed)
+    if args.moments == "bf16":  # one allocation each, 16-byte aligned
+        m, v = m.to(torch.bfloat16), v.to(torch.bfloat16)
     rq = [torch.empty(n, dtype=torch.int8, device=dev) for _ in range(P)]
     rs = [torch.empty(nb, dtype=torch.float32, device=dev) for _ in range(P)]
     words = torch.zeros(16, dtype=torch.uint8, device=dev)
-    a, keep = zdp.make_zpp_args(gq, gs, st[0], m, v, rq, rs, n=n, scale=wl.scale, t=1,
+    a, keep = zdp.make_zpp_args(gq, gs, w, m, v, rq, rs, n=n, scale=wl.scale, t=1,
                                 d_overflow=words[0:4].view(torch.int32),
                                 d_sumsq=words[8:16].view(torch.float64), moments=args.moments,
                                 **HP)
@@ -1172,7 +1182,7 @@ def run_unfused(args):
     grads = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
     for q in range(P):
         workloads.fill_grads(grads[q], wl, q, 0, args.seed)
-    st = torch.empty(3, P * S, dtype=torch.float32, device=dev)
+    _, *st = state_rows(P * S, dev)
     workloads.fill_state(st[0], st[1], st[2], wl, args.seed)
     shards = torch.empty(P * S, dtype=torch.float32, device=dev)
     reps = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]

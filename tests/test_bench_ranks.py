@@ -137,3 +137,17 @@ def test_flat_slice_workloads_by_name():
     assert workloads.by_name("flat_p8_32m").name == workloads.flat_p8_32m().name
     with pytest.raises(KeyError):
         workloads.by_name("flat_px_32m")
+
+
+def test_state_rows_start_on_256_byte_boundaries():
+    """The bench's master, m and v rows stay 16-byte aligned (the vector paths
+    need it) whatever P * S is, e.g. P = 3 on the 32M slice."""
+    import bench
+
+    for length in (1, 7, 33554433, 33554436):
+        buf, w, m, v = bench.state_rows(length, "cpu")
+        assert w.numel() == m.numel() == v.numel() == length
+        base = buf.data_ptr()
+        for row in (w, m, v):
+            assert (row.data_ptr() - base) % 256 == 0
+            assert row.is_contiguous()
