@@ -97,6 +97,13 @@ class StreamedStep:
                 moments=moments))
         self.producer = torch.cuda.Stream(device)
         self.stepper = torch.cuda.Stream(device)
+        # The buffers live on the two side streams: when they are freed, the
+        # caching allocator must wait for the work queued there, not only for
+        # the stream they were allocated on.
+        for bufset in self.bufs:
+            for x in bufset:
+                x.record_stream(self.producer)
+                x.record_stream(self.stepper)
         self.ready = [torch.cuda.Event() for _ in self.bounds]
         self.done = [torch.cuda.Event() for _ in self.bounds]
 
