@@ -71,6 +71,9 @@ unsigned long long current_context_id() {
 }
 
 int lookup_failed(cudaError_t e) {
+  // The failed lookup's error is reported here; clear it from the runtime so
+  // that a later call's launch check does not take it for its own.
+  if (e != cudaSuccess) cudaGetLastError();
   char msg[200];
   std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
   return zdp::report_error(ZDP_ERR_CUDA, msg);
