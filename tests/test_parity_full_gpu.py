@@ -173,6 +173,53 @@ def test_gpt_1p3b_bench_configuration(moments):
     _free()
 
 
+def test_gpt_1p3b_checked_step():
+    """The overflow-checked step on the 1.3B list as the benchmark runs it
+    (--check-overflow: two passes through the caller's workspace, the range
+    far above one resident wave).  A clean step matches the oracle at the
+    sampled indices; the next step, with one +inf injected into one rank's
+    gradient, raises the flag and leaves every sampled value of master, m, v
+    and the replicas as the clean step left it."""
+    wl = workloads.gpt_1p3b()
+    seed = 4
+    pb = Problem(wl, seed)
+    rng = np.random.default_rng(seed)
+    bad_q, bad_i = int(rng.integers(0, pb.P)), int(rng.integers(0, pb.n))
+    idx = sample_indices(pb.n, pb.S, pb.P, seed, extra=[t.offset for t in wl.tensors] + [bad_i],
+                         k_random=50_000, around=8)
+    idx_dev = torch.from_numpy(idx).to(DEV)
+    w, m, v = pb.oracle_state(idx_dev)
+    args, keep = zdp.make_step_args(pb.grads, *pb.buffers(), pb.replicas, n=pb.n,
+                                    scale=wl.scale, t=1, d_overflow=pb.flag, d_sumsq=pb.sumsq,
+                                    check_overflow=True, **HP)
+    ws = torch.empty(zdp.zdp_step_workspace_bytes(args), dtype=torch.uint8, device=DEV)
+    args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
+    rep = None
+    for t in (1, 2):
+        for q in range(pb.P):
+            workloads.fill_grads(pb.grads[q], wl, q, t, seed)
+        if t == 2:
+            pb.grads[bad_q].view(torch.int16)[bad_i] = 0x7F80  # bf16 +inf
+        gs = np.stack([gather_bits(g, idx_dev) for g in pb.grads])
+        pb.words.zero_()
+        args.t = t
+        zdp.zdp_step(args)
+        torch.cuda.synchronize()
+        # the flag first (on copies: skip=True leaves the state alone), then
+        # the step as the flag decides
+        _, _, flag = oracle.step_sampled(gs, idx, oracle.BF16, w.copy(), m.copy(), v.copy(),
+                                         pb.n, wl.scale, t=t, skip=True, **HP)
+        assert flag == (1 if t == 2 else 0)
+        assert int(pb.flag.item()) == flag
+        _, rep_t, _ = oracle.step_sampled(gs, idx, oracle.BF16, w, m, v, pb.n, wl.scale, t=t,
+                                          skip=bool(flag), **HP)
+        if not flag:
+            rep = rep_t  # a skipped step leaves the replicas as the clean step wrote them
+        pb.check(idx, idx_dev, w, m, v, rep, f"1.3B checked t={t}")
+    del pb, args, keep, ws
+    _free()
+
+
 def test_gpt_7b_streamed_buckets():
     # fp32 state (79 GB) and 8 replicas (105 GB) resident; each rank's
     # gradients regenerated one 256 MiB bucket at a time by a producer stream

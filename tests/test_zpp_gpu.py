@@ -233,7 +233,11 @@ def test_zpp_sub_ranges_compose_to_the_whole():
         assert_bits_equal(parts[6][q].cpu().numpy(), whole[6][q].cpu().numpy(), "scales")
 
 
-def test_zpp_on_the_1p3b_model_sampled_blocks():
+@pytest.mark.parametrize("moments", ["f32", "bf16"])
+def test_zpp_on_the_1p3b_model_sampled_blocks(moments):
+    """The bench's ZeRO++ configuration (1.3B list, P = 8), both moment types,
+    checked block by block against the oracle at 300 random blocks, the ends
+    and every shard edge."""
     wl = workloads.gpt_1p3b()
     P, n, seed = wl.P, wl.n, 9
     S = -(-n // P)
@@ -249,28 +253,44 @@ def test_zpp_on_the_1p3b_model_sampled_blocks():
         gs.append(sc)
     st = torch.empty(3, P * S, dtype=torch.float32, device=DEV)
     workloads.fill_state(st[0], st[1], st[2], wl, seed)
+    w, m, v = st[0], st[1], st[2]
+    if moments == "bf16":  # the same moments held in bf16, one allocation each
+        m, v = m.to(torch.bfloat16), v.to(torch.bfloat16)
+
+    def host(t, lo, hi):
+        return bits_of(t[lo:hi]).copy() if t.dtype == torch.bfloat16 else t[lo:hi].cpu().numpy().copy()
+
     rq = [torch.zeros(n, dtype=torch.int8, device=DEV) for _ in range(P)]
     rs = [torch.zeros(nb, dtype=torch.float32, device=DEV) for _ in range(P)]
     rng = np.random.default_rng(seed)
     blocks = sorted(set(rng.integers(0, nb, 300).tolist()) | {0, nb - 1} |
                     {(r * S) // 256 for r in range(1, P)})
-    before = {b: [st[k, b * 256:min(n, b * 256 + 256)].cpu().numpy().copy() for k in range(3)]
-              for b in blocks}
-    a, keep = zdp.make_zpp_args(gq, gs, st[0], st[1], st[2], rq, rs, n=n, scale=wl.scale, t=1,
-                                **HP)
+    before = {}
+    for b in blocks:
+        lo, hi = b * 256, min(n, b * 256 + 256)
+        before[b] = (host(w, lo, hi), host(m, lo, hi), host(v, lo, hi))
+    a, keep = zdp.make_zpp_args(gq, gs, w, m, v, rq, rs, n=n, scale=wl.scale, t=1,
+                                moments=moments, **HP)
     zdp.zdp_step_zpp(a)
     torch.cuda.synchronize()
     for b in blocks:
         lo, hi = b * 256, min(n, b * 256 + 256)
         g8 = np.stack([_i8(gq[q][lo:hi]) for q in range(P)])
         g8s = np.stack([gs[q][b:b + 1].cpu().numpy() for q in range(P)])
-        w, m, v = before[b]
+        ww, mm, vv = before[b]
         wq, wsc = np.zeros((P, hi - lo), np.int8), np.zeros((P, 1), np.float32)
-        oracle.step_zpp(g8, g8s, w, m, v, wq, wsc, n, lo, hi - lo, wl.scale, t=1, base=lo, **HP)
-        assert_state_close(st[0, lo:hi].cpu().numpy(), w, f"block {b} master")
-        assert_state_close(st[1, lo:hi].cpu().numpy(), m, f"block {b} m")
+        oracle.step_zpp(g8, g8s, ww, mm, vv, wq, wsc, n, lo, hi - lo, wl.scale, t=1, base=lo,
+                        moments=moments, **HP)
+        label = f"{moments} block {b}"
+        assert_state_close(host(w, lo, hi), ww, label + " master")
+        if moments == "f32":
+            assert_state_close(host(m, lo, hi), mm, label + " m")
+            assert_state_close(host(v, lo, hi), vv, label + " v")
+        else:
+            assert np.array_equal(host(m, lo, hi), mm), label + " m"
+            assert np.array_equal(host(v, lo, hi), vv), label + " v"
         for q in (0, P - 1):
-            assert np.array_equal(_i8(rq[q][lo:hi]), wq[q]), f"block {b} replica {q}"
+            assert np.array_equal(_i8(rq[q][lo:hi]), wq[q]), f"{label} replica {q}"
             assert rs[q][b].item() == wsc[q, 0]
 
 
