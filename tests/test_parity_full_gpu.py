@@ -220,6 +220,35 @@ def test_gpt_1p3b_checked_step():
     _free()
 
 
+def test_gpt_1p3b_unfused_chain():
+    """The step's three calls at the 1.3B size, as `bench.py --unfused` runs
+    them: reduce-scatter into fp32 shards, AdamW over the whole P*S range,
+    all-gather of the new master into the P replicas."""
+    wl = workloads.gpt_1p3b()
+    seed = 7
+    pb = Problem(wl, seed)
+    idx = sample_indices(pb.n, pb.S, pb.P, seed, extra=[t.offset for t in wl.tensors],
+                         k_random=50_000, around=8)
+    idx_dev = torch.from_numpy(idx).to(DEV)
+    w, m, v = pb.oracle_state(idx_dev)
+    for q in range(pb.P):
+        workloads.fill_grads(pb.grads[q], wl, q, 1, seed)
+    gs = np.stack([gather_bits(g, idx_dev) for g in pb.grads])
+    shards = torch.empty(pb.P * pb.S, dtype=torch.float32, device=DEV)
+    zdp.zdp_reduce_scatter(pb.grads, shards, pb.n, pb.P, wl.scale, d_overflow=pb.flag,
+                           d_sumsq=pb.sumsq)
+    zdp.zdp_adamw_shard(pb.state[0], pb.state[1], pb.state[2], shards, pb.P * pb.S, t=1, **HP)
+    zdp.zdp_all_gather(pb.state[0], pb.replicas, pb.n, pb.P)
+    torch.cuda.synchronize()
+    gout, rep, flag = oracle.step_sampled(gs, idx, oracle.BF16, w, m, v, pb.n, wl.scale, t=1,
+                                          **HP)
+    assert flag == 0 and int(pb.flag.item()) == 0
+    assert_bits_equal(gather_f32(shards, idx_dev), gout, "1.3B unfused reduced gradients")
+    pb.check(idx, idx_dev, w, m, v, rep, "1.3B unfused chain")
+    del pb, shards
+    _free()
+
+
 def test_gpt_7b_streamed_buckets():
     # fp32 state (79 GB) and 8 replicas (105 GB) resident; each rank's
     # gradients regenerated one 256 MiB bucket at a time by a producer stream
