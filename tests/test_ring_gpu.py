@@ -61,3 +61,48 @@ def test_ring_is_bit_identical_to_the_fused_step(P, n, fp16):
     assert_bits_equal(ring.replica_bits(), fused.replica_bits(), "ring vs fused replicas")
     assert int(ring.flag.item()) == int(fused.flag.item())
     assert float(ring.sumsq.item()) == pytest.approx(float(fused.sumsq.item()), rel=1e-12)
+
+
+@pytest.mark.parametrize("P,n", [(8, 1 << 28), (64, 1 << 26)])
+def test_ring_at_the_study_sizes(P, n):
+    """The sizes `bench.py --ring-study` times (flat n = 2^28 up to P = 16,
+    2^26 at P = 64), against the oracle at sampled indices: every shard edge
+    with its neighbours, the ends and random elements."""
+    from zero_gradient_reduce_gb300 import workloads
+
+    wl = workloads.Workload(f"flat_{n}_p{P}", P=P, n=n, tensors=workloads._flat(n),
+                            fresh_state=True)
+    seed = 11
+    S = -(-n // P)
+    grads = [workloads.fill_grads(torch.empty(n, dtype=torch.bfloat16, device="cuda"), wl, q, 0,
+                                  seed) for q in range(P)]
+    st = [torch.zeros(P * S, dtype=torch.float32, device="cuda") for _ in range(3)]
+    workloads.fill_state(st[0], st[1], st[2], wl, seed)
+    reps = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    words = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(seed)
+    pts = {0, n - 1} | {r * S + d for r in range(1, P) for d in range(-8, 8)}
+    pts |= set(rng.integers(0, n, 20_000).tolist())
+    idx = np.array(sorted(i for i in pts if 0 <= i < n), np.int64)
+    idx_dev = torch.from_numpy(idx).to("cuda")
+    w, m, v = (x.index_select(0, idx_dev).cpu().numpy().copy() for x in st)
+    gs = np.stack([g.index_select(0, idx_dev).view(torch.int16).cpu().numpy().view(np.uint16)
+                   for g in grads])
+    a, keep = zdp.make_step_args(grads, st[0], st[1], st[2], reps, n=n, scale=wl.scale, t=1,
+                                 d_overflow=words[0:4].view(torch.int32),
+                                 d_sumsq=words[8:16].view(torch.float64), **HP)
+    ws = torch.empty(zdp.zdp_step_ring_workspace_bytes(a), dtype=torch.uint8, device="cuda")
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    zdp.zdp_step_ring(a)
+    torch.cuda.synchronize()
+    _, rep, flag = oracle.step_sampled(gs, idx, oracle.BF16, w, m, v, n, wl.scale, t=1, **HP)
+    label = f"ring P={P} n={n}"
+    assert flag == 0 and int(words[0:4].view(torch.int32).item()) == 0
+    assert_state_close(st[0].index_select(0, idx_dev).cpu().numpy(), w, label + " master")
+    assert_state_close(st[1].index_select(0, idx_dev).cpu().numpy(), m, label + " m")
+    assert_state_close(st[2].index_select(0, idx_dev).cpu().numpy(), v, label + " v")
+    for q in (0, P // 2, P - 1):
+        got = reps[q].index_select(0, idx_dev).view(torch.int16).cpu().numpy().view(np.uint16)
+        assert_bf16_close(got, rep, f"{label} replica {q}")
+    del grads, st, reps, ws, a, keep
+    torch.cuda.empty_cache()
