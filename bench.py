@@ -1329,8 +1329,9 @@ def overlap_measure(wl, dev, seed, steps, warmup, stream_times=True):
            "hidden_ms": prod_ms + step_ms - wall, "step_under_contention_ms": under,
            "step_bytes": bytes_per_param(P) * n, "overflow_flag": flag,
            "producer": "seeded N(0, sigma) bf16 gradients drawn bucket by bucket "
-                       "(workloads.fill_bucket_grads: one torch normal_ per rank and tensor "
-                       "slice), standing in for the backward pass"}
+                       "(workloads.fill_bucket_grads: one torch normal_ per rank and bucket, "
+                       "per tensor slice where sigma varies by tensor), standing in for the "
+                       "backward pass"}
     del ss, state, replicas
     torch.cuda.empty_cache()
     return out
