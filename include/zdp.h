@@ -203,9 +203,9 @@ size_t zdp_step_workspace_bytes(const zdp_step_args* args);
  * ZDP_TEST_COOP_EXTRA_ARRIVALS=k (tests only) makes the barrier wait for k
  * arrivals that never come, and ZDP_TEST_COOP_OVERSIZE=k (tests only) asks
  * for a cooperative grid k blocks larger than one resident wave, which the
- * runtime refuses, so that the two-pass fallback runs.  The skip decision covers this call's
- * range only; a caller streaming one step through several calls and wanting
- * a step-wide skip must check every range first (e.g. with
+ * runtime refuses, so that the two-pass fallback runs.  The skip decision
+ * covers this call's range only; a caller streaming one step through several
+ * calls and wanting a step-wide skip must check every range first (e.g. with
  * zdp_reduce_scatter into a scratch buffer).  A skipped step leaves t to the
  * caller: do not advance it. */
 int zdp_step(const zdp_step_args* args, void* stream);
